@@ -1,0 +1,225 @@
+/*
+ * moe.h -- C ABI of libmoe: the forward pass of one Mixture-of-Experts FFN
+ * layer on one NVIDIA B300 (sm_103a).
+ *
+ * The layer (pages cited by title and section):
+ *   router      z = x W_r^T (+ b)          «为什么MoE有效？稀疏激活的数学直觉与工程实践» §2.2;
+ *                                           «DeepSeek-V2 ...» summary §2.2 (expert_bias)
+ *   softmax     p = softmax(z) in fp32      same sections
+ *   top-k       k largest p, gates renormalised to sum 1 (ties -> lower expert index)
+ *   capacity    C = floor(floor(k N / E) * alpha); overflow dropped in token order
+ *               or rerouted to the next-best expert with room
+ *                                           «大模型MoE架构揭秘：如何用2%参数实现万亿级算力调度» §3.1, §4.2
+ *   experts     SwiGLU  y = (silu(x Wg^T) * (x Wu^T)) Wd^T   (same page, §3.2)
+ *               GELU    y = GELU(x W1^T + b1) W2^T + b2       («为什么MoE有效？» §3 code)
+ *               plus S shared experts applied to every token  («DeepSeek-V2 ...» summary §2.3)
+ *   combine     y_t = sum_s shared_s(x_t) + sum_j g_tj * expert_{e_tj}(x_t)
+ *                                           («为什么MoE有效？» §2.1)
+ *   statistics  expert_freq, mean_prob, L_bal = E * sum_e freq_e * P_e
+ *                                           («DeepSeek-V2 ...» summary §2.2 load_balance_loss)
+ *
+ * Conventions for every call:
+ *   - Every tensor pointer is a DEVICE pointer, allocated and owned by the
+ *     caller.  The library allocates and frees nothing.
+ *   - `stream` is a cudaStream_t (passed as void*).  Calls enqueue work on it
+ *     and return without synchronising, except moe_device_status().
+ *   - A call returns MOE_OK after enqueueing, or a negative moe_status from the
+ *     host-side checks done before any launch; then nothing was written.
+ *     A failed launch returns MOE_ERR_CUDA.
+ *   - Device-side failures (a bounded wait that ran out) are recorded in a
+ *     status word inside the workspace; read it with moe_device_status().
+ *   - Layouts are row-major.  Weight matrices are nn.Linear style [out, in].
+ *     Shared experts are experts E .. E+S-1 of the expert weight arrays.
+ *   - dtype MOE_BF16: x, w_router, expert weights, x_perm, y_perm and y are
+ *     bf16; router_bias, probabilities and gates are fp32.  MOE_F32: all fp32.
+ *   - Alignment: every pointer 16-byte aligned; for bf16, d_model and d_ff are
+ *     multiples of 8 (16-byte rows for the tensor-memory-access engine).
+ *   - Integer outputs are bit-exact and deterministic; float outputs are
+ *     deterministic run to run (no floating-point atomics anywhere).
+ *
+ * Expert-row space.  Dispatch sorts assignments into one segment per routed
+ * expert e (rows offsets[e] .. offsets[e]+counts[e]-1, padded up to a multiple
+ * of MOE_SEGMENT_ALIGN rows), followed by one segment of n_tokens rows per
+ * shared expert (row offsets[E+s] + t holds token t).  x_perm holds the routed
+ * rows; y_perm holds routed and shared rows.  Padding rows hold unspecified
+ * values and are never read by the combine.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,   /* null/misaligned pointer, bad size or field     */
+  MOE_ERR_UNSUPPORTED = -2,   /* valid but not implemented (e.g. bf16 + GELU)    */
+  MOE_ERR_WORKSPACE = -3,     /* workspace smaller than moe_workspace_size()     */
+  MOE_ERR_CUDA = -4,          /* a CUDA runtime call or launch failed            */
+  MOE_ERR_TIMEOUT = -5,       /* a device-side bounded wait ran out              */
+  MOE_ERR_DEVICE = -6         /* another device-side check failed                */
+} moe_status;
+
+typedef enum { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1 } moe_act;
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+typedef enum { MOE_CAP_NONE = 0, MOE_CAP_DROP = 1, MOE_CAP_REROUTE = 2 } moe_cap_mode;
+
+#define MOE_MAX_EXPERTS 256      /* routed experts E                      */
+#define MOE_MAX_TOPK 8           /* k <= min(E, 8)                        */
+#define MOE_MAX_SHARED 8         /* shared experts S                      */
+#define MOE_MAX_TOKENS (1 << 22) /* N                                     */
+#define MOE_SEGMENT_ALIGN 128    /* rows; segment starts are multiples    */
+
+/* Layer shape and options (plain values, read on the host only). */
+typedef struct moe_config {
+  int32_t n_tokens;        /* N >= 0 (N = 0 is a no-op)                    */
+  int32_t d_model;         /* d >= 1                                       */
+  int32_t n_experts;       /* E routed experts, 1 .. MOE_MAX_EXPERTS       */
+  int32_t top_k;           /* k, 1 .. min(E, MOE_MAX_TOPK)                 */
+  int32_t d_ff;            /* F, expert hidden width                       */
+  int32_t n_shared;        /* S, 0 .. MOE_MAX_SHARED                       */
+  int32_t act;             /* moe_act                                      */
+  int32_t dtype;           /* moe_dtype                                    */
+  int32_t cap_mode;        /* moe_cap_mode                                 */
+  float alpha;             /* capacity factor (> 0 unless MOE_CAP_NONE)    */
+  int32_t has_ffn_bias;    /* GELU experts: b1 [E+S, F], b2 [E+S, d]       */
+  int32_t has_router_bias; /* router_bias [E] fp32 is added to the logits  */
+} moe_config;
+
+/* Statistics outputs (device pointers; each may be NULL = not written). */
+typedef struct moe_stats {
+  float* expert_freq;  /* [E]  pre-capacity top-k picks of e / (N k)          */
+  float* mean_prob;    /* [E]  (1/N) sum_t p[t,e]                              */
+  float* l_bal;        /* [1]  E * sum_e expert_freq[e] * mean_prob[e]         */
+  int32_t* counts;     /* [E]  assignments kept per routed expert (post-cap)  */
+  int32_t* n_dropped;  /* [1]  assignments dropped by capacity                */
+  int32_t* n_rerouted; /* [1]  assignments moved to another expert            */
+} moe_stats;
+
+/* Optional stage timing for moe_forward: cudaEvent_t handles (as void*),
+ * recorded on `stream` before the router [0], after the router [1], after
+ * dispatch [2], after the first expert GEMM [3], after the second expert GEMM
+ * [4] and after the combine [5].  NULL entries are skipped. */
+typedef struct moe_timing {
+  void* events[6];
+} moe_timing;
+
+/* Device pointers into a moe_forward workspace (for inspection and tests). */
+typedef struct moe_views {
+  int32_t* topk_idx;  /* [N, k]   */
+  float* topk_w;      /* [N, k]   */
+  float* probs;       /* [N, E]   (written only when cap_mode == REROUTE) */
+  int32_t* final_idx; /* [N, k]   */
+  int32_t* pos;       /* [N, k]   */
+  int32_t* offsets;   /* [E+S+1]  */
+  int32_t* perm;      /* [max_rows] */
+  void* x_perm;       /* [max_rows, d]        */
+  void* h;            /* [max_total_rows, F]  */
+  void* y_perm;       /* [max_total_rows, d]  */
+} moe_views;
+
+/* ---- host-only queries (no device work, no CUDA context needed) ---------- */
+
+/* Text for a moe_status value. */
+const char* moe_status_string(int status);
+
+/* MOE_OK if the configuration is valid and implemented, else the status. */
+int moe_validate_config(const moe_config* cfg);
+
+/* Expert capacity C = floor(floor(k*N/E) * alpha) for DROP/REROUTE, -1 for
+ * MOE_CAP_NONE or an invalid config («大模型MoE架构揭秘» §3.1). */
+int32_t moe_capacity(const moe_config* cfg);
+
+/* Routed rows of x_perm/perm including segment padding (upper bound). */
+int64_t moe_max_rows(const moe_config* cfg);
+
+/* Rows of y_perm (routed + shared segments, with padding). */
+int64_t moe_max_total_rows(const moe_config* cfg);
+
+/* Bytes of device workspace that every call below needs (0 on error).  The
+ * same size serves every call; 256-byte aligned. */
+size_t moe_workspace_size(const moe_config* cfg);
+
+/* Pointers into a workspace laid out by moe_forward. */
+int moe_workspace_views(const moe_config* cfg, void* workspace, size_t workspace_bytes,
+                        moe_views* out);
+
+/* ---- device calls ---------------------------------------------------------- */
+
+/* Router: logits, fp32 softmax, top-k with renormalised gates, and the
+ * pre-capacity statistics (expert_freq, mean_prob, l_bal).
+ *   x        [N, d]      w_router [E, d]      router_bias [E] fp32 (NULL unless
+ *   has_router_bias)
+ *   topk_idx [N, k] int32 out, slot 0 = most probable expert
+ *   topk_w   [N, k] fp32  out, renormalised gates (sum 1 per token)
+ *   probs    [N, E] fp32  out, nullable
+ *   stats    nullable; expert_freq, mean_prob, l_bal are written if non-NULL. */
+int moe_route(const moe_config* cfg, const void* x, const void* w_router,
+              const float* router_bias, int32_t* topk_idx, float* topk_w, float* probs,
+              const moe_stats* stats, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Dispatch: per-expert histogram, scan, capacity (drop or reroute), segment
+ * layout and the permutation of token rows into x_perm.
+ *   topk_idx  [N, k] int32 in (as written by moe_route)
+ *   probs     [N, E] fp32 in, required when cap_mode == REROUTE (candidate
+ *             order), else may be NULL
+ *   x         [N, d] in
+ *   final_idx [N, k] int32 out: expert of the slot after capacity, -1 dropped
+ *   pos       [N, k] int32 out: row of the slot in the expert-row space, -1 dropped
+ *   offsets   [E+S+1] int32 out: segment start rows; offsets[E+S] = total rows
+ *   perm      [moe_max_rows] int32 out: token of each routed row, -1 on padding
+ *   x_perm    [moe_max_rows, d] out: x_perm[pos[t,j]] = x[t]
+ *   stats     nullable; counts, n_dropped, n_rerouted are written if non-NULL.
+ * Within a routed expert, rows are its kept assignments in ascending token
+ * order, then rerouted ones in (round, token, slot) order. */
+int moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const float* probs,
+                 const void* x, int32_t* final_idx, int32_t* pos, int32_t* offsets,
+                 int32_t* perm, void* x_perm, const moe_stats* stats, void* workspace,
+                 size_t workspace_bytes, void* stream);
+
+/* Expert FFNs of every segment as one grouped computation.
+ *   x       [N, d]   in (rows of the shared-expert segments)
+ *   x_perm  [moe_max_rows, d] in (rows of the routed segments)
+ *   offsets [E+S+1]  in (segment layout from moe_dispatch; every segment
+ *           length a multiple of MOE_SEGMENT_ALIGN except as produced there)
+ *   w_gate  [E+S, F, d]  SwiGLU gate weight | GELU W1
+ *   w_up    [E+S, F, d]  SwiGLU up weight   | GELU: NULL
+ *   w_down  [E+S, d, F]  down weight (W2)
+ *   b1 [E+S, F], b2 [E+S, d]  GELU biases (NULL unless has_ffn_bias)
+ *   y_perm  [moe_max_total_rows, d] out
+ * bf16 runs on the tensor cores (fp32 accumulation, the SwiGLU product is
+ * rounded to bf16 between the two GEMMs); fp32 runs in fp32 on the CUDA cores. */
+int moe_expert_ffn(const moe_config* cfg, const void* x, const void* x_perm,
+                   const int32_t* offsets, const void* w_gate, const void* w_up,
+                   const void* w_down, const void* b1, const void* b2, void* y_perm,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Combine: y[t] = sum_s y_perm[offsets[E+s] + t] + sum_j topk_w[t,j] *
+ * y_perm[pos[t,j]] over kept slots, summed in fp32 in that fixed order.
+ *   y [N, d] out (dtype). */
+int moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* offsets,
+                const int32_t* final_idx, const int32_t* pos, const float* topk_w, void* y,
+                void* stream);
+
+/* The whole layer: route -> dispatch -> expert FFNs -> combine, all on
+ * `stream`, intermediates in `workspace` (see moe_workspace_views).
+ *   y [N, d] out; stats nullable; timing nullable. */
+int moe_forward(const moe_config* cfg, const void* x, const void* w_router,
+                const float* router_bias, const void* w_gate, const void* w_up,
+                const void* w_down, const void* b1, const void* b2, void* y,
+                const moe_stats* stats, void* workspace, size_t workspace_bytes,
+                void* stream, const moe_timing* timing);
+
+/* Synchronises `stream`, then copies the workspace's device status word to
+ * *status_out (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE) and clears it. */
+int moe_device_status(void* workspace, void* stream, int32_t* status_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

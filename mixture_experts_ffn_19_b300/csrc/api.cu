@@ -1,0 +1,343 @@
+// C ABI of libmoe (declared in include/moe.h): argument checks, workspace
+// layout, and the launch sequence of the layer on one stream.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "moe.h"
+
+namespace moe {
+namespace {
+
+constexpr size_t kWsAlign = 256;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+int64_t align_rows(int64_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Layout {
+  size_t status, topk_idx, topk_w, probs, final_idx, slot, pos, offsets, perm;
+  size_t psum_part, picks_part, chunk_cnt, local_rank, pend;
+  size_t x_perm, h, y_perm, total;
+};
+
+int64_t max_rows_of(const moe_config* c) {
+  return (int64_t)c->n_tokens * c->top_k + (int64_t)c->n_experts * (kAlign - 1);
+}
+int64_t max_total_rows_of(const moe_config* c) {
+  return max_rows_of(c) + (int64_t)c->n_shared * align_rows(c->n_tokens);
+}
+
+Layout layout_of(const moe_config* c) {
+  Layout L;
+  const size_t N = (size_t)c->n_tokens, k = (size_t)c->top_k, E = (size_t)c->n_experts;
+  const size_t es = c->dtype == MOE_BF16 ? 2 : 4;
+  const size_t rblocks = (N + kRouteTM - 1) / kRouteTM;
+  const size_t chunks = (N + kRankTC - 1) / kRankTC;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { const size_t o = off; off = align_up(off + bytes, kWsAlign); return o; };
+  L.status = take(sizeof(int32_t));
+  L.topk_idx = take(N * k * 4);
+  L.topk_w = take(N * k * 4);
+  L.probs = take(N * E * 4);
+  L.final_idx = take(N * k * 4);
+  L.slot = take(N * k * 4);
+  L.pos = take(N * k * 4);
+  L.offsets = take((E + c->n_shared + 1) * 4);
+  L.perm = take((size_t)max_rows_of(c) * 4);
+  L.psum_part = take(rblocks * E * 4);
+  L.picks_part = take(rblocks * E * 4);
+  L.chunk_cnt = take(chunks * E * 4);
+  L.local_rank = take(N * k * 4);
+  L.pend = take(N * 4);
+  L.x_perm = take((size_t)max_rows_of(c) * c->d_model * es);
+  L.h = take((size_t)max_total_rows_of(c) * c->d_ff * es);
+  L.y_perm = take((size_t)max_total_rows_of(c) * c->d_model * es);
+  L.total = off;
+  return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
+
+int capacity_of(const moe_config* c) {
+  if (c->cap_mode == MOE_CAP_NONE) return INT32_MAX;
+  const double base = (double)(((int64_t)c->top_k * c->n_tokens) / c->n_experts);
+  const double cap = floor(base * (double)c->alpha);
+  return cap >= (double)INT32_MAX ? INT32_MAX : (int)cap;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+  return n;
+}
+
+int check_ws(const moe_config* c, const void* ws, size_t bytes) {
+  if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (bytes < layout_of(c).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+void record(const moe_timing* t, int i, cudaStream_t s) {
+  if (t && t->events[i]) cudaEventRecord(static_cast<cudaEvent_t>(t->events[i]), s);
+}
+
+int route_impl(const moe_config* c, const void* x, const void* w_router, const float* bias,
+               int32_t* topk_idx, float* topk_w, float* probs, const moe_stats* stats, void* ws,
+               cudaStream_t s) {
+  const Layout L = layout_of(c);
+  RouteParams rp{x, w_router, c->has_router_bias ? bias : nullptr, c->n_tokens, c->d_model,
+                 c->n_experts, c->top_k, topk_idx, topk_w, probs,
+                 at<float>(ws, L.psum_part), at<int32_t>(ws, L.picks_part)};
+  if (launch_route(rp, c->dtype == MOE_BF16, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (stats && (stats->expert_freq || stats->mean_prob || stats->l_bal)) {
+    RouteStatsParams sp{rp.psum_part, rp.picks_part, (c->n_tokens + kRouteTM - 1) / kRouteTM,
+                        c->n_tokens, c->n_experts, c->top_k, stats->expert_freq,
+                        stats->mean_prob, stats->l_bal};
+    if (launch_route_stats(sp, s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+int dispatch_impl(const moe_config* c, const int32_t* topk_idx, const float* probs, const void* x,
+                  int32_t* final_idx, int32_t* pos, int32_t* offsets, int32_t* perm, void* x_perm,
+                  const moe_stats* stats, void* ws, cudaStream_t s) {
+  const Layout L = layout_of(c);
+  DispatchParams dp{};
+  dp.N = c->n_tokens; dp.E = c->n_experts; dp.k = c->top_k; dp.S = c->n_shared;
+  dp.d = c->d_model; dp.cap_mode = c->cap_mode; dp.C = capacity_of(c);
+  dp.n_chunks = (c->n_tokens + kRankTC - 1) / kRankTC;
+  dp.topk_idx = topk_idx; dp.probs = probs; dp.x = x;
+  dp.chunk_cnt = at<int32_t>(ws, L.chunk_cnt);
+  dp.local_rank = at<int32_t>(ws, L.local_rank);
+  dp.final_idx = final_idx; dp.slot = at<int32_t>(ws, L.slot); dp.pos = pos;
+  dp.offsets = offsets; dp.perm = perm; dp.x_perm = x_perm;
+  dp.pend = at<int32_t>(ws, L.pend);
+  dp.counts = stats ? stats->counts : nullptr;
+  dp.n_dropped = stats ? stats->n_dropped : nullptr;
+  dp.n_rerouted = stats ? stats->n_rerouted : nullptr;
+  dp.status = at<int>(ws, L.status);
+  return launch_dispatch(dp, c->dtype == MOE_BF16, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int ffn_impl(const moe_config* c, const void* x, const void* x_perm, const int32_t* offsets,
+             const void* w_gate, const void* w_up, const void* w_down, const void* b1,
+             const void* b2, void* y_perm, void* ws, cudaStream_t s, cudaEvent_t mid) {
+  const Layout L = layout_of(c);
+  FfnParams fp{};
+  fp.N = c->n_tokens; fp.d = c->d_model; fp.F = c->d_ff; fp.E = c->n_experts;
+  fp.S = c->n_shared; fp.act = c->act; fp.offsets = offsets; fp.x = x; fp.x_perm = x_perm;
+  fp.w_gate = w_gate; fp.w_up = w_up; fp.w_down = w_down;
+  fp.b1 = c->has_ffn_bias ? b1 : nullptr; fp.b2 = c->has_ffn_bias ? b2 : nullptr;
+  fp.h = at<void>(ws, L.h); fp.y_perm = y_perm;
+  fp.max_rows = max_rows_of(c); fp.max_total_rows = max_total_rows_of(c);
+  fp.status = at<int>(ws, L.status);
+  fp.num_sms = num_sms();
+  const cudaError_t err = c->dtype == MOE_BF16 ? launch_ffn_tc(fp, s, mid) : launch_ffn_simt(fp, s, mid);
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int combine_impl(const moe_config* c, const void* y_perm, const int32_t* offsets,
+                 const int32_t* final_idx, const int32_t* pos, const float* topk_w, void* y,
+                 cudaStream_t s) {
+  CombineParams cp{c->n_tokens, c->d_model, c->n_experts, c->top_k, c->n_shared,
+                   y_perm, offsets, final_idx, pos, topk_w, y};
+  return launch_combine(cp, c->dtype == MOE_BF16, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(int st) {
+  switch (st) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE: return "device-side check failed";
+    default: return "unknown status";
+  }
+}
+
+int moe_validate_config(const moe_config* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->n_tokens < 0 || c->n_tokens > MOE_MAX_TOKENS) return MOE_ERR_INVALID_ARG;
+  if (c->d_model < 8 || c->d_model % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (c->d_ff < 8 || c->d_ff % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (c->n_experts < 1 || c->n_experts > MOE_MAX_EXPERTS) return MOE_ERR_INVALID_ARG;
+  if (c->top_k < 1 || c->top_k > std::min(c->n_experts, MOE_MAX_TOPK)) return MOE_ERR_INVALID_ARG;
+  if (c->n_shared < 0 || c->n_shared > MOE_MAX_SHARED) return MOE_ERR_INVALID_ARG;
+  if (c->act != MOE_ACT_GELU && c->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->cap_mode < MOE_CAP_NONE || c->cap_mode > MOE_CAP_REROUTE) return MOE_ERR_INVALID_ARG;
+  if (c->cap_mode != MOE_CAP_NONE && !(c->alpha > 0.f && isfinite(c->alpha)))
+    return MOE_ERR_INVALID_ARG;
+  if (c->has_ffn_bias && c->act != MOE_ACT_GELU) return MOE_ERR_UNSUPPORTED;
+  if (c->dtype == MOE_BF16 && (c->act == MOE_ACT_GELU || c->has_ffn_bias)) return MOE_ERR_UNSUPPORTED;
+  if (max_total_rows_of(c) >= INT32_MAX) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+int32_t moe_capacity(const moe_config* c) {
+  if (moe_validate_config(c) != MOE_OK || c->cap_mode == MOE_CAP_NONE) return -1;
+  return capacity_of(c);
+}
+
+int64_t moe_max_rows(const moe_config* c) {
+  return moe_validate_config(c) == MOE_OK ? max_rows_of(c) : -1;
+}
+
+int64_t moe_max_total_rows(const moe_config* c) {
+  return moe_validate_config(c) == MOE_OK ? max_total_rows_of(c) : -1;
+}
+
+size_t moe_workspace_size(const moe_config* c) {
+  return moe_validate_config(c) == MOE_OK ? layout_of(c).total : 0;
+}
+
+int moe_workspace_views(const moe_config* c, void* ws, size_t bytes, moe_views* out) {
+  int st = moe_validate_config(c);
+  if (st != MOE_OK) return st;
+  if (!out) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(c, ws, bytes)) != MOE_OK) return st;
+  const Layout L = layout_of(c);
+  out->topk_idx = at<int32_t>(ws, L.topk_idx);
+  out->topk_w = at<float>(ws, L.topk_w);
+  out->probs = at<float>(ws, L.probs);
+  out->final_idx = at<int32_t>(ws, L.final_idx);
+  out->pos = at<int32_t>(ws, L.pos);
+  out->offsets = at<int32_t>(ws, L.offsets);
+  out->perm = at<int32_t>(ws, L.perm);
+  out->x_perm = at<void>(ws, L.x_perm);
+  out->h = at<void>(ws, L.h);
+  out->y_perm = at<void>(ws, L.y_perm);
+  return MOE_OK;
+}
+
+int moe_route(const moe_config* c, const void* x, const void* w_router, const float* bias,
+              int32_t* topk_idx, float* topk_w, float* probs, const moe_stats* stats, void* ws,
+              size_t ws_bytes, void* stream) {
+  int st = moe_validate_config(c);
+  if (st != MOE_OK) return st;
+  if ((st = check_ws(c, ws, ws_bytes)) != MOE_OK) return st;
+  if (!x || !w_router || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (c->has_router_bias && !bias) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(at<int>(ws, layout_of(c).status), 0, sizeof(int), s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (c->n_tokens == 0) return MOE_OK;
+  return route_impl(c, x, w_router, bias, topk_idx, topk_w, probs, stats, ws, s);
+}
+
+int moe_dispatch(const moe_config* c, const int32_t* topk_idx, const float* probs, const void* x,
+                 int32_t* final_idx, int32_t* pos, int32_t* offsets, int32_t* perm, void* x_perm,
+                 const moe_stats* stats, void* ws, size_t ws_bytes, void* stream) {
+  int st = moe_validate_config(c);
+  if (st != MOE_OK) return st;
+  if ((st = check_ws(c, ws, ws_bytes)) != MOE_OK) return st;
+  if (!topk_idx || !x || !final_idx || !pos || !offsets || !perm || !x_perm)
+    return MOE_ERR_INVALID_ARG;
+  if (c->cap_mode == MOE_CAP_REROUTE && !probs) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_INVALID_ARG;
+  if (c->n_tokens == 0) return MOE_OK;
+  return dispatch_impl(c, topk_idx, probs, x, final_idx, pos, offsets, perm, x_perm, stats, ws,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int moe_expert_ffn(const moe_config* c, const void* x, const void* x_perm, const int32_t* offsets,
+                   const void* w_gate, const void* w_up, const void* w_down, const void* b1,
+                   const void* b2, void* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  int st = moe_validate_config(c);
+  if (st != MOE_OK) return st;
+  if ((st = check_ws(c, ws, ws_bytes)) != MOE_OK) return st;
+  if (!x || !x_perm || !offsets || !w_gate || !w_down || !y_perm) return MOE_ERR_INVALID_ARG;
+  if (c->act == MOE_ACT_SWIGLU && !w_up) return MOE_ERR_INVALID_ARG;
+  if (c->has_ffn_bias && (!b1 || !b2)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x_perm) || !aligned16(w_gate) || !aligned16(w_down) ||
+      !aligned16(y_perm) || (w_up && !aligned16(w_up)))
+    return MOE_ERR_INVALID_ARG;
+  if (c->n_tokens == 0) return MOE_OK;
+  return ffn_impl(c, x, x_perm, offsets, w_gate, w_up, w_down, b1, b2, y_perm, ws,
+                  static_cast<cudaStream_t>(stream), nullptr);
+}
+
+int moe_combine(const moe_config* c, const void* y_perm, const int32_t* offsets,
+                const int32_t* final_idx, const int32_t* pos, const float* topk_w, void* y,
+                void* stream) {
+  int st = moe_validate_config(c);
+  if (st != MOE_OK) return st;
+  if (!y_perm || !offsets || !final_idx || !pos || !topk_w || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  if (c->n_tokens == 0) return MOE_OK;
+  return combine_impl(c, y_perm, offsets, final_idx, pos, topk_w, y,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int moe_forward(const moe_config* c, const void* x, const void* w_router, const float* bias,
+                const void* w_gate, const void* w_up, const void* w_down, const void* b1,
+                const void* b2, void* y, const moe_stats* stats, void* ws, size_t ws_bytes,
+                void* stream, const moe_timing* timing) {
+  int st = moe_validate_config(c);
+  if (st != MOE_OK) return st;
+  if ((st = check_ws(c, ws, ws_bytes)) != MOE_OK) return st;
+  if (!x || !w_router || !w_gate || !w_down || !y) return MOE_ERR_INVALID_ARG;
+  if (c->act == MOE_ACT_SWIGLU && !w_up) return MOE_ERR_INVALID_ARG;
+  if (c->has_router_bias && !bias) return MOE_ERR_INVALID_ARG;
+  if (c->has_ffn_bias && (!b1 || !b2)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(w_gate) || !aligned16(w_down) ||
+      !aligned16(y) || (w_up && !aligned16(w_up)))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Layout L = layout_of(c);
+  if (cudaMemsetAsync(at<int>(ws, L.status), 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (c->n_tokens == 0) return MOE_OK;
+  float* probs = c->cap_mode == MOE_CAP_REROUTE ? at<float>(ws, L.probs) : nullptr;
+  record(timing, 0, s);
+  st = route_impl(c, x, w_router, bias, at<int32_t>(ws, L.topk_idx), at<float>(ws, L.topk_w),
+                  probs, stats, ws, s);
+  if (st != MOE_OK) return st;
+  record(timing, 1, s);
+  st = dispatch_impl(c, at<int32_t>(ws, L.topk_idx), probs, x, at<int32_t>(ws, L.final_idx),
+                     at<int32_t>(ws, L.pos), at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.perm),
+                     at<void>(ws, L.x_perm), stats, ws, s);
+  if (st != MOE_OK) return st;
+  record(timing, 2, s);
+  st = ffn_impl(c, x, at<void>(ws, L.x_perm), at<int32_t>(ws, L.offsets), w_gate, w_up, w_down,
+                b1, b2, at<void>(ws, L.y_perm), ws, s,
+                timing ? static_cast<cudaEvent_t>(timing->events[3]) : nullptr);
+  if (st != MOE_OK) return st;
+  record(timing, 4, s);
+  st = combine_impl(c, at<void>(ws, L.y_perm), at<int32_t>(ws, L.offsets),
+                    at<int32_t>(ws, L.final_idx), at<int32_t>(ws, L.pos), at<float>(ws, L.topk_w),
+                    y, s);
+  if (st != MOE_OK) return st;
+  record(timing, 5, s);
+  return MOE_OK;
+}
+
+int moe_device_status(void* ws, void* stream, int32_t* status_out) {
+  if (!ws || !status_out) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  *status_out = v == kDevOk ? MOE_OK : (v == kDevTimeout ? MOE_ERR_TIMEOUT : MOE_ERR_DEVICE);
+  return MOE_OK;
+}
+
+}  // extern "C"

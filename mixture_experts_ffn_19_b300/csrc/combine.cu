@@ -1,0 +1,94 @@
+// Combine: y[t] = sum_s shared_s(x_t) + sum_j g_tj * expert_{e_tj}(x_t).
+//
+// «为什么MoE有效？稀疏激活的数学直觉与工程实践» §2.1 (y = sum_i g_i(x) Expert_i(x))
+// and §3 code (output[token_indices] += w * expert_output); «DeepSeek-V2 ...»
+// summary §2.3 (layer output = shared-expert output + gated routed output).
+//
+// A gather, not a scatter: each token reads its own k + S rows of y_perm and
+// sums them in fp32 in a fixed order (shared experts, then slots 0..k-1), so
+// the result is deterministic without atomics.  One CTA per token, 16-byte
+// vectors across d.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+template <typename T>
+struct Vec;  // 16 bytes of T as fp32 lanes
+
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int n = 8;
+  __device__ static void load(const uint4& u, float (&f)[8]) {
+    f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x); f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+    f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z); f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
+  }
+  __device__ static uint4 store(const float (&f)[8]) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+  }
+};
+
+template <>
+struct Vec<float> {
+  static constexpr int n = 4;
+  __device__ static void load(const uint4& u, float (&f)[4]) {
+    f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+  }
+  __device__ static uint4 store(const float (&f)[4]) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
+  constexpr int VN = Vec<T>::n;
+  const int t = blockIdx.x;
+  __shared__ int rows[kMaxTopk + 8];
+  __shared__ float gates[kMaxTopk + 8];
+  __shared__ int nrows;
+  if (threadIdx.x == 0) {
+    int n = 0;
+    for (int s = 0; s < p.S; ++s) { rows[n] = p.offsets[p.E + s] + t; gates[n] = 1.f; ++n; }
+    for (int j = 0; j < p.k; ++j) {
+      const size_t a = (size_t)t * p.k + j;
+      if (p.final_idx[a] >= 0) { rows[n] = p.pos[a]; gates[n] = p.topk_w[a]; ++n; }
+    }
+    nrows = n;
+  }
+  __syncthreads();
+  const int nvec = p.d / VN;
+  const uint4* src = static_cast<const uint4*>(p.y_perm);
+  uint4* dst = static_cast<uint4*>(p.y);
+  const int n = nrows;
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+    float acc[VN];
+#pragma unroll
+    for (int q = 0; q < VN; ++q) acc[q] = 0.f;
+    for (int r = 0; r < n; ++r) {
+      float f[VN];
+      Vec<T>::load(src[(size_t)rows[r] * nvec + v], f);
+      const float g = gates[r];
+#pragma unroll
+      for (int q = 0; q < VN; ++q) acc[q] = fmaf(g, f[q], acc[q]);
+    }
+    dst[(size_t)t * nvec + v] = Vec<T>::store(acc);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineParams& p, bool bf16, cudaStream_t s) {
+  const int vn = bf16 ? 8 : 4;
+  const int nvec = p.d / vn;
+  int threads = nvec < 256 ? ((nvec + 31) / 32) * 32 : 256;
+  if (bf16) combine_kernel<__nv_bfloat16><<<p.N, threads, 0, s>>>(p);
+  else combine_kernel<float><<<p.N, threads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -16,3 +16,16 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="session")
+def cuda():
+    """Skip when no CUDA device is visible; otherwise make sure libmoe.so is built."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mixture_experts_ffn_19_b300 import build
+    build.build()
+    import mixture_experts_ffn_19_b300 as moe
+    moe.lib()
+    return torch.device("cuda:0")

@@ -1,0 +1,93 @@
+"""The C-ABI library loads, exports every declared entry point, and its host-side
+logic (validation, capacity, sizing) behaves; no device work is done here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixture_experts_ffn_19_b300 as moe
+from mixture_experts_ffn_19_b300 import build as moe_build
+import oracle
+import synth
+from helpers import config_of
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe_build.build()
+    return moe.lib()
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(moe_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "moe_forward" in names and "moe_route" in names and len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), n
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_validation(lib):
+    good = config_of(synth.WORKLOADS["mixtral_prefill"])
+    assert moe.moe_validate_config(good) == moe.MOE_OK
+    for field, bad, want in [("n_experts", 0, moe.MOE_ERR_INVALID_ARG),
+                             ("n_experts", 257, moe.MOE_ERR_INVALID_ARG),
+                             ("top_k", 9, moe.MOE_ERR_INVALID_ARG),
+                             ("top_k", 0, moe.MOE_ERR_INVALID_ARG),
+                             ("d_model", 4100, moe.MOE_ERR_INVALID_ARG),
+                             ("d_ff", 12, moe.MOE_ERR_INVALID_ARG),
+                             ("n_tokens", -1, moe.MOE_ERR_INVALID_ARG),
+                             ("cap_mode", 3, moe.MOE_ERR_INVALID_ARG),
+                             ("alpha", 0.0, moe.MOE_ERR_INVALID_ARG),
+                             ("act", moe.MOE_ACT_GELU, moe.MOE_ERR_UNSUPPORTED)]:
+        c = config_of(synth.WORKLOADS["mixtral_prefill"])
+        setattr(c, field, bad)
+        assert moe.moe_validate_config(c) == want, field
+    small = config_of(synth.WORKLOADS["tiny_fp32"])
+    small.top_k = 9
+    assert moe.moe_validate_config(small) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_workspace_size(small) == 0
+
+
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_capacity_matches_oracle(lib, name):
+    w = synth.WORKLOADS[name]
+    c = config_of(w)
+    want = oracle.capacity(w.n_tokens, w.n_experts, w.top_k, w.alpha) if w.cap_mode else -1
+    assert moe.moe_capacity(c) == want
+    # the worked example of the capacity section: N=32, E=64, k=2, alpha=1.2 -> 1
+    c2 = moe.make_config(32, 64, 64, 2, 64, cap_mode=moe.MOE_CAP_DROP, alpha=1.2)
+    assert moe.moe_capacity(c2) == 1
+
+
+def test_sizes(lib):
+    w = synth.WORKLOADS["dsv2"]
+    c = config_of(w)
+    assert moe.moe_max_rows(c) == w.n_tokens * w.top_k + w.n_experts * 127
+    assert moe.moe_max_total_rows(c) == moe.moe_max_rows(c) + 2 * 8192
+    assert moe.moe_workspace_size(c) % 256 == 0
+    assert moe.moe_workspace_size(c) > moe.moe_max_total_rows(c) * w.d_model * 2
+
+
+def test_null_arguments_are_rejected_before_any_launch(lib):
+    c = config_of(synth.WORKLOADS["tiny_fp32"])
+    st = lib.moe_route(ctypes.byref(c), None, None, None, None, None, None, None, None, 0, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    st = lib.moe_forward(ctypes.byref(c), None, None, None, None, None, None, None, None, None,
+                         None, None, 0, None, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    st = lib.moe_combine(ctypes.byref(c), None, None, None, None, None, None, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    assert moe.status_string(moe.MOE_ERR_WORKSPACE) == "workspace too small"

@@ -1,0 +1,121 @@
+"""Whole-layer parity: CUDA moe_forward vs oracle.moe_forward on the same inputs."""
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_ffn_19_b300 as moe
+import oracle
+import synth
+from helpers import config_of, rel_err_inf, to_dev, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def run_forward(w, inp, device, with_views=False):
+    cfg = config_of(w)
+    ws = moe.alloc_workspace(cfg, device)
+    E = w.n_experts
+    xd = to_dev(inp["x"])
+    y = torch.zeros((w.n_tokens, w.d_model), dtype=xd.dtype, device=device)
+    stats = {n: torch.zeros(E if n in ("expert_freq", "mean_prob", "counts") else 1,
+                            dtype=torch.int32 if n in ("counts", "n_dropped", "n_rerouted") else torch.float32,
+                            device=device)
+             for n in ("expert_freq", "mean_prob", "l_bal", "counts", "n_dropped", "n_rerouted")}
+    st = moe.make_stats(**stats)
+    moe.moe_forward(cfg, xd, to_dev(inp["w_router"]), to_dev(inp["router_bias"]),
+                    to_dev(inp["w_gate"]), to_dev(inp["w_up"]), to_dev(inp["w_down"]),
+                    to_dev(inp["b1"]), to_dev(inp["b2"]), y, st, ws)
+    assert moe.moe_device_status(ws) == moe.MOE_OK
+    out = {"y": y, "stats": {k: v.cpu().numpy() for k, v in stats.items()}}
+    if with_views:
+        out["ws"] = ws
+        out["views"] = moe.moe_workspace_views(cfg, ws)
+    return out
+
+
+def view_i32(ws, ptr, n):
+    base = ws.data_ptr()
+    off = (ptr - base) // 4
+    return ws.view(torch.int32)[off:off + n].cpu().numpy()
+
+
+def view_f32(ws, ptr, n):
+    base = ws.data_ptr()
+    off = (ptr - base) // 4
+    return ws.view(torch.float32)[off:off + n].cpu().numpy()
+
+
+def check_forward(w, inp, g, tokens=None):
+    o = oracle.moe_forward(w, inp, tokens=tokens)
+    N, k = w.n_tokens, w.top_k
+    ws, v = g["ws"], g["views"]
+    idx = view_i32(ws, v.topk_idx, N * k).reshape(N, k)
+    final = view_i32(ws, v.final_idx, N * k).reshape(N, k)
+    near = o["margin"] < 1e-6
+    routing_same = np.all(idx == o["idx"], axis=1) & np.all(final == o["final"], axis=1)
+    bad = np.nonzero(~routing_same)[0]
+    print(f"{w.name}: near-ties {near.sum()}, routing mismatches {len(bad)}")
+    if near.sum() == 0:
+        assert len(bad) == 0, f"routing differs on tokens {bad[:10]}"
+    toks = o["tokens"]
+    y = to_f64(g["y"])[toks]
+    keep = routing_same[toks]
+    err = rel_err_inf(y[keep], o["y"][keep])
+    tol = 1e-4 if w.dtype == synth.DT_F32 else 2e-2
+    print(f"{w.name}: y rel err {err:.3g} over {keep.sum()} tokens")
+    assert err <= tol
+    s = g["stats"]
+    np.testing.assert_allclose(s["mean_prob"], o["mean_prob"], rtol=1e-5, atol=1e-9)
+    np.testing.assert_allclose(s["l_bal"][0], o["l_bal"], rtol=1e-5)
+    if len(bad) == 0:
+        np.testing.assert_array_equal(s["counts"], o["counts"])
+        assert s["n_dropped"][0] == o["n_dropped"] and s["n_rerouted"][0] == o["n_rerouted"]
+    return o
+
+
+SMALL = [
+    synth.small_workload("tiny_fp32"),
+    synth.small_workload("mixtral_prefill", n_tokens=700, d_model=256, d_ff=512, alpha=0.8),
+    synth.small_workload("dsv2", n_tokens=400, d_model=320, n_experts=20, top_k=6, d_ff=192),
+    synth.small_workload("e64_reroute", n_tokens=2048, d_model=256, d_ff=256, alpha=1.0),
+    synth.small_workload("decode_mixtral", d_model=512, d_ff=1024),
+    synth.small_workload("decode_dsv2", d_model=256, d_ff=256),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_forward_small(cuda, w):
+    inp = synth.make_inputs(w)
+    check_forward(w, inp, run_forward(w, inp, cuda, with_views=True))
+
+
+def test_forward_is_deterministic(cuda):
+    w = synth.small_workload("e64_reroute", n_tokens=2048, d_model=256, d_ff=256, alpha=1.0)
+    inp = synth.make_inputs(w)
+    a = run_forward(w, inp, cuda)["y"]
+    b = run_forward(w, inp, cuda)["y"]
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_forward_edge_cases(cuda):
+    cases = [
+        synth.small_workload("mixtral_prefill", n_tokens=1, d_model=64, n_experts=1, top_k=1, d_ff=64),
+        synth.small_workload("mixtral_prefill", n_tokens=5, d_model=64, n_experts=4, top_k=4, d_ff=64),
+        synth.small_workload("dsv2", n_tokens=3, d_model=64, n_experts=64, top_k=2, d_ff=64, n_shared=1),
+        synth.small_workload("tiny_fp32", n_tokens=1, n_experts=1, top_k=1),
+    ]
+    for w in cases:
+        inp = synth.make_inputs(w)
+        check_forward(w, inp, run_forward(w, inp, cuda, with_views=True))
+
+
+def test_forward_zero_tokens(cuda):
+    w = synth.small_workload("mixtral_prefill", n_tokens=0, d_model=64, d_ff=64)
+    cfg = config_of(w)
+    ws = moe.alloc_workspace(cfg, cuda)
+    inp = synth.make_inputs(w.replace(n_tokens=1))
+    y = torch.zeros((1, 64), dtype=torch.bfloat16, device=cuda)
+    moe.moe_forward(cfg, to_dev(inp["x"]), to_dev(inp["w_router"]), None, to_dev(inp["w_gate"]),
+                    to_dev(inp["w_up"]), to_dev(inp["w_down"]), None, None, y, None, ws)
+    assert moe.moe_device_status(ws) == moe.MOE_OK
+    assert torch.count_nonzero(y) == 0
