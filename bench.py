@@ -1,0 +1,360 @@
+"""Benchmark of the MoE-FFN forward layer on B300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline]
+
+A step is one moe_forward (router -> dispatch -> expert GEMMs -> combine) over
+one batch of the workload, inputs resident in HBM.  L2 is flushed between
+steps (a 512 MB write, outside the timed events).  With --gpus N > 1 (launched
+by torch.distributed.run) every rank runs an independent replica on its own
+GPU: the layer has no exchange step in this build, so there is no collective
+on the data path; the barrier and the max over ranks of the timed region are
+the only cross-rank steps.
+
+--impl reference times the CPU oracle (float64 NumPy) on the host cores on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer fwd tokens/s @1 B300; grouped-GEMM TFLOP/s & HBM GB/s vs roofline"
+HEADLINE = "mixtral_prefill"
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p["bf16_tflops_sustained"], "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+                "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def layer_work(w, counts_kept, n_dropped):
+    """Algorithmic FLOPs of one forward (kept assignments and shared rows only)."""
+    N, d, E, k, F, S = w.n_tokens, w.d_model, w.n_experts, w.top_k, w.d_ff, w.n_shared
+    rows = int(counts_kept) + S * N
+    g1 = 2.0 * rows * d * (2 * F if w.act == synth.ACT_SWIGLU else F)
+    g2 = 2.0 * rows * F * d
+    router = 2.0 * N * d * E
+    return {"rows": rows, "gemm1_flop": g1, "gemm2_flop": g2, "router_flop": router,
+            "total_flop": g1 + g2 + router}
+
+
+def to_dev(a, device):
+    import torch
+    if a is None:
+        return None
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def run_cpu_oracle(w, inp, budget_s=20.0, max_tokens=None):
+    """Time the oracle (as it stands) on a bounded token sample; returns tokens/s."""
+    import oracle
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+    except Exception:
+        cores = os.cpu_count() or 1
+    # size the sample from a one-token probe so the run stays near the budget
+    t0 = time.perf_counter()
+    oracle.moe_forward(w, inp, tokens=np.arange(1))
+    probe = time.perf_counter() - t0
+    n = max(1, min(w.n_tokens, int(budget_s / max(probe, 1e-3))))
+    if max_tokens:
+        n = min(n, max_tokens)
+    t0 = time.perf_counter()
+    oracle.moe_forward(w, inp, tokens=np.arange(n))
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "tokens/s", "cores": int(cores), "kind": "oracle",
+            "sample": f"routing and capacity over all {w.n_tokens} tokens, expert FFNs and "
+                      f"combine for the first {n} tokens ({dt:.1f} s)"}
+
+
+def bench_reference(args, w):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    inp = synth.make_inputs(w)
+    budget = args.ref_budget if args.ref_budget else max(2.0, 150.0 / (args.warmup + args.steps))
+    per_step = []
+    info = None
+    for i in range(args.warmup + args.steps):
+        r = run_cpu_oracle(w, inp, budget_s=budget, max_tokens=args.ref_tokens)
+        if i >= args.warmup:
+            per_step.append(r["value"])
+            info = r
+    value = statistics.mean(per_step)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * w.n_tokens / value, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, world),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": info["cores"],
+                             "kind": "oracle", "sample": info["sample"]},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, world):
+    return {"workload": w.name, "n_tokens": w.n_tokens, "d_model": w.d_model,
+            "n_experts": w.n_experts, "top_k": w.top_k, "d_ff": w.d_ff, "n_shared": w.n_shared,
+            "activation": "swiglu" if w.act == synth.ACT_SWIGLU else "gelu",
+            "capacity": ["none", "drop", "reroute"][w.cap_mode],
+            "alpha": w.alpha if w.cap_mode else None, "router_bias": w.bias_law,
+            "l2_flush": True, "parallelism": f"replicas{world}" if world > 1 else "single"}
+
+
+def bench_ours(args, w):
+    import torch
+    import mixture_experts_ffn_19_b300 as moe
+    rank, local, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = moe.make_config(w.n_tokens, w.d_model, w.n_experts, w.top_k, w.d_ff, w.n_shared,
+                          act=w.act, dtype=w.dtype, cap_mode=w.cap_mode, alpha=w.alpha,
+                          has_ffn_bias=w.has_ffn_bias, has_router_bias=w.has_router_bias)
+    inp = synth.make_inputs(w)
+    x = to_dev(inp["x"], dev)
+    wr = to_dev(inp["w_router"], dev)
+    rb = to_dev(inp["router_bias"], dev)
+    wg, wu, wd = (to_dev(inp[k], dev) for k in ("w_gate", "w_up", "w_down"))
+    b1, b2 = to_dev(inp["b1"], dev), to_dev(inp["b2"], dev)
+    y = torch.empty((w.n_tokens, w.d_model), dtype=x.dtype, device=dev)
+    ws = moe.alloc_workspace(cfg, dev)
+    E = w.n_experts
+    st_t = {"expert_freq": torch.zeros(E, device=dev), "mean_prob": torch.zeros(E, device=dev),
+            "l_bal": torch.zeros(1, device=dev),
+            "counts": torch.zeros(E, dtype=torch.int32, device=dev),
+            "n_dropped": torch.zeros(1, dtype=torch.int32, device=dev),
+            "n_rerouted": torch.zeros(1, dtype=torch.int32, device=dev)}
+    stats = moe.make_stats(**st_t)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    args_f = (cfg, x, wr, rb, wg, wu, wd, b1, b2, y)
+
+    # warm-up
+    for _ in range(args.warmup):
+        moe.moe_forward(*args_f, stats, ws, stream)
+    torch.cuda.synchronize()
+    if moe.moe_device_status(ws) != moe.MOE_OK:
+        raise RuntimeError("device status not ok after warm-up")
+    kept = int(st_t["counts"].sum())
+    nd = int(st_t["n_dropped"][0])
+    work = layer_work(w, kept, nd)
+
+    # timed region: K steps, per-step and per-stage CUDA events, L2 flush between steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    timings = []
+    for s in range(args.steps):
+        t = moe.moe_timing()
+        for i in range(6):
+            evs[s][i].record(stream)          # torch creates the CUDA event on first record
+            t.events[i] = evs[s][i].cuda_event
+        timings.append(t)
+    torch.cuda.synchronize()
+    assert all(e.cuda_event for row in evs for e in row)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(dev.index)
+    with ClockSampler(gpu_id) as clk:
+        for s in range(args.steps):
+            flush.fill_(s & 0xFF)
+            moe.moe_forward(*args_f, stats, ws, stream, timing=timings[s])
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    step_ms = [evs[s][0].elapsed_time(evs[s][5]) for s in range(args.steps)]
+    stage = {n: [evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps)]
+             for i, n in enumerate(["route", "dispatch", "gemm1", "gemm2", "combine"])}
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t[0])
+    st = moe.moe_device_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status {moe.status_string(st)}")
+
+    # end to end through the public API with host buffers: pinned H2D of x, forward,
+    # D2H of y, all inside the events
+    x_host = torch.from_numpy(inp["x"].view(np.int16) if inp["x"].dtype == np.uint16
+                              else inp["x"]).pin_memory()
+    y_host = torch.empty((w.n_tokens, w.d_model), dtype=torch.int16 if w.dtype else torch.float32
+                         ).pin_memory()
+    x_in = torch.empty_like(x)
+    e2e_ms = []
+    for s in range(args.warmup + args.steps):
+        flush.fill_(s & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        x_in.view(x_host.dtype).copy_(x_host, non_blocking=True)
+        moe.moe_forward(cfg, x_in, wr, rb, wg, wu, wd, b1, b2, y, stats, ws, stream)
+        y_host.copy_(y.view(y_host.dtype), non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if s >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_total = sum(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t[0])
+
+    pk = peaks()
+    g1_ms = statistics.mean(stage["gemm1"])
+    g1_tflops = work["gemm1_flop"] / (g1_ms * 1e-3) / 1e12
+    peak_t = pk["bf16_tflops_sustained"]
+    tokens_total = w.n_tokens * args.steps * world
+    value = tokens_total / (total_ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == synth.DT_BF16 else "f32", "data": "synthetic",
+        "config": workload_config(w, world),
+        "roofline": {"bound": "tensor", "kernel": "ffn_tc_kernel<0> (gate/up GEMM + SwiGLU)",
+                     "achieved": g1_tflops, "peak": peak_t, "unit": "TFLOP/s",
+                     "frac": g1_tflops / peak_t, "traffic": None,
+                     "peak_source": f"{pk['source']} bf16 sustained",
+                     "algorithmic_flop_per_launch": work["gemm1_flop"]},
+        "e2e": {"value": w.n_tokens * args.steps * world / (e2e_total * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(x.numel() * x.element_size()),
+                "d2h_bytes_per_step": int(y.numel() * y.element_size())},
+        "gpu_launches": 8 * args.steps,
+        "clocks": clk.summary(),
+        "stages_ms": {k: statistics.mean(v) for k, v in stage.items()},
+        "layer_tflops": work["total_flop"] / (total_ms / args.steps * 1e-3) / 1e12,
+        "kept_assignments": kept, "dropped": nd,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = run_cpu_oracle(w, inp, budget_s=args.ref_budget or 15.0,
+                                              max_tokens=args.ref_tokens)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=list(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=None,
+                    help="seconds of oracle work per step (default: ~150 s over the run, "
+                         "15 s for the cpu_baseline leg)")
+    ap.add_argument("--ref-tokens", type=int, default=None)
+    ap.add_argument("--set", action="append", default=[], metavar="FIELD=VALUE",
+                    help="override a workload field (e.g. n_experts=2) for a smaller case")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    w = synth.WORKLOADS[args.workload]
+    for kv in args.set:
+        key, val = kv.split("=", 1)
+        cur = getattr(w, key)
+        w = w.replace(**{key: type(cur)(float(val)) if isinstance(cur, (int, float)) else val},
+                      name=w.name + f"[{key}={val}]")
+    if args.impl == "reference":
+        return bench_reference(args, w)
+    return bench_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
