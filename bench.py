@@ -20,7 +20,6 @@ import argparse
 import json
 import os
 import statistics
-import subprocess
 import sys
 import threading
 import time
@@ -53,60 +52,78 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """SM clock and clock-event (throttle) reasons sampled through NVML every
+    10 ms while the timed region runs (read-only queries)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+               "sw_power_cap": 0x4}
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.lines = []
+    def __init__(self, torch_device):
+        self.dev = torch_device
+        self.samples = []
+        self.reasons = set()
+        self.max_mhz = None
+        self.stop = threading.Event()
+        self.handle = None
+
+    def _handle(self):
+        import pynvml
+        pynvml.nvmlInit()
+        import torch
+        props = torch.cuda.get_device_properties(self.dev)
+        bus = getattr(props, "pci_bus_id", None)
+        if bus is not None:
+            dom = getattr(props, "pci_domain_id", 0)
+            devid = getattr(props, "pci_device_id", 0)
+            try:
+                return pynvml.nvmlDeviceGetHandleByPciBusId(f"{dom:08x}:{bus:02x}:{devid:02x}.0")
+            except Exception:
+                pass
+        try:
+            return pynvml.nvmlDeviceGetHandleByUUID("GPU-" + str(props.uuid))
+        except Exception:
+            pass
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        idx = int(vis.split(",")[self.dev.index or 0]) if vis and vis.split(",")[0].isdigit() \
+            else (self.dev.index or 0)
+        return pynvml.nvmlDeviceGetHandleByIndex(idx)
+
+    def _run(self):
+        import pynvml
+        while not self.stop.is_set():
+            try:
+                self.samples.append(pynvml.nvmlDeviceGetClockInfo(self.handle, pynvml.NVML_CLOCK_SM))
+                r = pynvml.nvmlDeviceGetCurrentClocksEventReasons(self.handle)
+                for n, bit in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(n)
+            except Exception:
+                pass
+            time.sleep(0.01)
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            import pynvml
+            self.handle = self._handle()
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.handle, pynvml.NVML_CLOCK_SM)
+            self.thread = threading.Thread(target=self._run, daemon=True)
             self.thread.start()
-        except Exception:
-            self.proc = None
+        except Exception as exc:  # clocks are reported as unavailable
+            self.error = repr(exc)
+            self.handle = None
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def __exit__(self, *a):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except Exception:
-                self.proc.kill()
+        self.stop.set()
+        if self.handle is not None:
+            self.thread.join(timeout=2)
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                    "samples": 0, "error": getattr(self, "error", "no samples")}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
 
 
 def layer_work(w, counts_kept, n_dropped):
@@ -137,16 +154,17 @@ def run_cpu_oracle(w, inp, budget_s=20.0, max_tokens=None):
         cores = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
     except Exception:
         cores = os.cpu_count() or 1
-    # size the sample from a one-token probe so the run stays near the budget
-    t0 = time.perf_counter()
-    oracle.moe_forward(w, inp, tokens=np.arange(1))
-    probe = time.perf_counter() - t0
-    n = max(1, min(w.n_tokens, int(budget_s / max(probe, 1e-3))))
-    if max_tokens:
-        n = min(n, max_tokens)
-    t0 = time.perf_counter()
-    oracle.moe_forward(w, inp, tokens=np.arange(n))
-    dt = time.perf_counter() - t0
+    # grow the token sample until one timed run takes about a third of the budget
+    n, dt = 1, 0.0
+    while True:
+        t0 = time.perf_counter()
+        oracle.moe_forward(w, inp, tokens=np.arange(n))
+        dt = time.perf_counter() - t0
+        if dt >= budget_s / 3 or n >= w.n_tokens or (max_tokens and n >= max_tokens):
+            break
+        n = min(w.n_tokens, max(2 * n, int(n * budget_s / 3 / max(dt, 1e-3))))
+        if max_tokens:
+            n = min(n, max_tokens)
     return {"value": n / dt, "unit": "tokens/s", "cores": int(cores), "kind": "oracle",
             "sample": f"routing and capacity over all {w.n_tokens} tokens, expert FFNs and "
                       f"combine for the first {n} tokens ({dt:.1f} s)"}
@@ -156,23 +174,28 @@ def bench_reference(args, w):
     rank, _, world = dist_env()
     if rank != 0:
         return 0
+    import oracle
     inp = synth.make_inputs(w)
-    budget = args.ref_budget if args.ref_budget else max(2.0, 150.0 / (args.warmup + args.steps))
+    budget = args.ref_budget if args.ref_budget else min(15.0, max(1.0, 150.0 / (args.warmup + args.steps)))
+    info = run_cpu_oracle(w, inp, budget_s=3 * budget, max_tokens=args.ref_tokens)
+    n = int(info["sample"].split("first ")[1].split(" ")[0])
     per_step = []
-    info = None
     for i in range(args.warmup + args.steps):
-        r = run_cpu_oracle(w, inp, budget_s=budget, max_tokens=args.ref_tokens)
+        t0 = time.perf_counter()
+        oracle.moe_forward(w, inp, tokens=np.arange(n))
+        dt = time.perf_counter() - t0
         if i >= args.warmup:
-            per_step.append(r["value"])
-            info = r
-    value = statistics.mean(per_step)
+            per_step.append(dt)
+    value = n * len(per_step) / sum(per_step)
+    sample = (f"routing and capacity over all {w.n_tokens} tokens, expert FFNs and combine "
+              f"for the first {n} tokens, {statistics.mean(per_step):.2f} s per step")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1000.0 * w.n_tokens / value, "higher_is_better": True,
+            "ms_per_step": 1000.0 * statistics.mean(per_step), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(w, world),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": info["cores"],
-                             "kind": "oracle", "sample": info["sample"]},
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -244,11 +267,7 @@ def bench_ours(args, w):
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
-    try:
-        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        gpu_id = str(dev.index)
-    with ClockSampler(gpu_id) as clk:
+    with ClockSampler(dev) as clk:
         for s in range(args.steps):
             flush.fill_(s & 0xFF)
             moe.moe_forward(*args_f, stats, ws, stream, timing=timings[s])
@@ -331,8 +350,8 @@ def bench_ours(args, w):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE, choices=list(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -22,7 +22,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Layout {
   size_t status, topk_idx, topk_w, probs, final_idx, slot, pos, offsets, perm;
-  size_t psum_part, picks_part, chunk_cnt, local_rank, pend;
+  size_t part, psum_part, picks_part, chunk_cnt, local_rank, pend, rr_state, rr_scratch;
   size_t x_perm, h, y_perm, total;
 };
 
@@ -37,7 +37,8 @@ Layout layout_of(const moe_config* c) {
   Layout L;
   const size_t N = (size_t)c->n_tokens, k = (size_t)c->top_k, E = (size_t)c->n_experts;
   const size_t es = c->dtype == MOE_BF16 ? 2 : 4;
-  const size_t rblocks = (N + kRouteTM - 1) / kRouteTM;
+  const size_t rblocks = (size_t)route_finish_blocks(c->n_tokens);
+  const RouteSplit rs = route_split(c->n_tokens, c->d_model, c->dtype == MOE_BF16);
   const size_t chunks = (N + kRankTC - 1) / kRankTC;
   size_t off = 0;
   auto take = [&](size_t bytes) { const size_t o = off; off = align_up(off + bytes, kWsAlign); return o; };
@@ -50,11 +51,14 @@ Layout layout_of(const moe_config* c) {
   L.pos = take(N * k * 4);
   L.offsets = take((E + c->n_shared + 1) * 4);
   L.perm = take((size_t)max_rows_of(c) * 4);
+  L.part = take((size_t)rs.ks * N * E * 4);
   L.psum_part = take(rblocks * E * 4);
   L.picks_part = take(rblocks * E * 4);
   L.chunk_cnt = take(chunks * E * 4);
   L.local_rank = take(N * k * 4);
   L.pend = take(N * 4);
+  L.rr_state = take(sizeof(RerouteState));
+  L.rr_scratch = take(reroute_scratch_ints(c->n_tokens, c->top_k, c->n_experts) * 4);
   L.x_perm = take((size_t)max_rows_of(c) * c->d_model * es);
   L.h = take((size_t)max_total_rows_of(c) * c->d_ff * es);
   L.y_perm = take((size_t)max_total_rows_of(c) * c->d_model * es);
@@ -94,11 +98,11 @@ int route_impl(const moe_config* c, const void* x, const void* w_router, const f
                cudaStream_t s) {
   const Layout L = layout_of(c);
   RouteParams rp{x, w_router, c->has_router_bias ? bias : nullptr, c->n_tokens, c->d_model,
-                 c->n_experts, c->top_k, topk_idx, topk_w, probs,
-                 at<float>(ws, L.psum_part), at<int32_t>(ws, L.picks_part)};
+                 c->n_experts, c->top_k, topk_idx, topk_w, probs, at<float>(ws, L.part),
+                 at<float>(ws, L.psum_part), at<int32_t>(ws, L.picks_part), at<int>(ws, L.status)};
   if (launch_route(rp, c->dtype == MOE_BF16, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (stats && (stats->expert_freq || stats->mean_prob || stats->l_bal)) {
-    RouteStatsParams sp{rp.psum_part, rp.picks_part, (c->n_tokens + kRouteTM - 1) / kRouteTM,
+    RouteStatsParams sp{rp.psum_part, rp.picks_part, route_finish_blocks(c->n_tokens),
                         c->n_tokens, c->n_experts, c->top_k, stats->expert_freq,
                         stats->mean_prob, stats->l_bal};
     if (launch_route_stats(sp, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -120,6 +124,10 @@ int dispatch_impl(const moe_config* c, const int32_t* topk_idx, const float* pro
   dp.final_idx = final_idx; dp.slot = at<int32_t>(ws, L.slot); dp.pos = pos;
   dp.offsets = offsets; dp.perm = perm; dp.x_perm = x_perm;
   dp.pend = at<int32_t>(ws, L.pend);
+  dp.rr = at<RerouteState>(ws, L.rr_state);
+  dp.rr_prop = at<int32_t>(ws, L.rr_scratch);
+  dp.rr_rank = dp.rr_prop + (size_t)c->n_tokens * c->top_k;
+  dp.rr_chunk = dp.rr_rank + (size_t)c->n_tokens * c->top_k;
   dp.counts = stats ? stats->counts : nullptr;
   dp.n_dropped = stats ? stats->n_dropped : nullptr;
   dp.n_rerouted = stats ? stats->n_rerouted : nullptr;

@@ -5,20 +5,26 @@
 // C = floor(k N / E) x alpha; overflow forced to the next-best expert), §4.2
 // code (an expert keeps its first C tokens in ascending token order).
 //
-// Three kernels, no atomics on anything whose order matters:
+// Kernels, no atomics on anything whose order matters:
 //   rank    one CTA per 256 tokens: a per-expert bitmap of the CTA's tokens
 //           gives each assignment its rank among earlier tokens of the CTA
 //           (popcount of the lower bits) and the CTA's per-expert count.
-//   plan    one CTA: per-expert exclusive scan over the token chunks (so an
-//           assignment's rank within its expert is chunk base + local rank,
-//           i.e. its position in token order), capacity, the reroute rounds,
-//           segment offsets, counts and drop/reroute totals.
+//   plan    one CTA: per-expert exclusive scan over the token chunks, so an
+//           assignment's rank within its expert is chunk base + local rank
+//           (its position in token order); capacity; segment offsets, counts
+//           and drop totals.  With reroute it instead marks the overflow
+//           pending and lists the tokens that have pending slots.
+//   reroute (reroute only) one cooperative launch of co-resident CTAs running
+//           the rounds, phases separated by a bounded grid barrier:
+//             A  every pending slot proposes the most probable expert (ties to
+//                the lower index) that was not full when the round started and
+//                that its token neither holds nor proposed earlier in the
+//                round (slots in slot order); bitmap ranks per chunk of tokens
+//             B  per-expert scan over the chunks; next fill levels
+//             C  an expert accepts proposals in token order while it has room
+//           then the segment layout, as plan does for the other modes.
 //   scatter one CTA per token: final expert, row, perm entry, and the 16-byte
 //           vector copy of x[t] into every row the token owns.
-// Reroute rounds: each pending slot proposes the most probable expert (ties to
-// the lower index) that was not full when the round started and that its token
-// neither holds nor proposed earlier in the round, slots in slot order; each
-// expert accepts proposals in ascending token order while it has room.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -28,6 +34,30 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 constexpr int kPendingMark = -2;
+constexpr int kRrThreads = 128;     // reroute CTA = one chunk of 128 pending tokens
+constexpr int kRrWords = kRrThreads / 32;
+
+__device__ __forceinline__ bool valid_expert(int e, int E) { return e >= 0 && e < E; }
+
+// In-place exclusive scan of column e of a row-major [n, E] int matrix by one
+// warp (32 rows per step, shuffle scan); returns the column total.  Loads go
+// through L2 so values written by other CTAs of a cooperative launch are seen.
+__device__ int warp_exclusive_scan_column(int32_t* m, int n, int E, int e, int lane) {
+  int carry = 0;
+  for (int r0 = 0; r0 < n; r0 += 32) {
+    const int r = r0 + lane;
+    const int v = r < n ? __ldcg(&m[(size_t)r * E + e]) : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (r < n) m[(size_t)r * E + e] = carry + incl - v;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return carry;
+}
 
 __global__ void __launch_bounds__(kRankTC) dispatch_rank_kernel(DispatchParams p) {
   extern __shared__ uint32_t bits[];             // [E][kRankTC/32]
@@ -41,7 +71,7 @@ __global__ void __launch_bounds__(kRankTC) dispatch_rank_kernel(DispatchParams p
   if (t < p.N) {
     for (int j = 0; j < k; ++j) {
       int e = p.topk_idx[(size_t)t * k + j];
-      if (e < 0 || e >= E) {          // not an expert index: record it, never index with it
+      if (!valid_expert(e, E)) {        // not an expert index: record it, never index with it
         set_status(p.status, kDevBadState);
         e = -1;
       }
@@ -67,193 +97,255 @@ __global__ void __launch_bounds__(kRankTC) dispatch_rank_kernel(DispatchParams p
   }
 }
 
-// Block-wide compaction of `n` candidates in order: writes the kept ones to
-// out[] (which may alias the source as long as out index <= source index).
-// Returns the number kept (same value in every thread).
-template <typename Pred, typename Val>
-__device__ int block_compact(int n, Pred keep, Val value, int32_t* out, int* warp_tot, int* total) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int base = 0;
-  for (int c0 = 0; c0 < n; c0 += kPlanThreads) {
-    const int i = c0 + tid;
-    const bool f = (i < n) && keep(i);
-    const int v = (i < n) ? value(i) : 0;
-    const uint32_t bal = __ballot_sync(0xffffffffu, f);
-    if (lane == 0) warp_tot[warp] = __popc(bal);
-    __syncthreads();
-    if (tid == 0) {
-      int run = 0;
-      for (int w = 0; w < kPlanThreads / 32; ++w) { const int c = warp_tot[w]; warp_tot[w] = run; run += c; }
-      *total = run;
-    }
-    __syncthreads();
-    if (f) out[base + warp_tot[warp] + __popc(bal & lanemask_lt())] = v;
-    base += *total;
-    __syncthreads();
-  }
-  return base;
-}
-
-__global__ void __launch_bounds__(kPlanThreads) dispatch_plan_kernel(DispatchParams p) {
-  extern __shared__ uint32_t dyn[];
-  const int E = p.E, k = p.k, N = p.N, S = p.S, C = p.C;
-  uint32_t* bits = dyn;                                         // [E][32]
-  int* pre = reinterpret_cast<int*>(dyn + E * 32);              // [E][32]
-  __shared__ int fill[kMaxExperts], total[kMaxExperts];
-  __shared__ int prop_cnt[kMaxExperts], chunk_tot[kMaxExperts];
-  __shared__ unsigned char full_s[kMaxExperts];
-  __shared__ int warp_tot[kPlanThreads / 32];
-  __shared__ int s_total, s_any, s_npend;
-  const int tid = threadIdx.x, lane = tid & 31;
-
-  // 1. per-expert exclusive scan over token chunks
-  for (int e = tid; e < E; e += kPlanThreads) {
-    int run = 0;
-    for (int c = 0; c < p.n_chunks; ++c) {
-      const int v = p.chunk_cnt[(size_t)c * E + e];
-      p.chunk_cnt[(size_t)c * E + e] = run;
-      run += v;
-    }
-    total[e] = run;
-    fill[e] = min(run, C);
-  }
-  __syncthreads();
-
-  if (p.cap_mode == 2) {
-    // 2. primary pass: keep rank < C, mark the rest pending
-    for (int a = tid; a < N * k; a += kPlanThreads) {
-      const int t = a / k;
-      const int e = p.topk_idx[a];
-      if (e < 0 || e >= E) { p.final_idx[a] = -1; p.slot[a] = -1; continue; }
-      const int rank = p.chunk_cnt[(size_t)(t / kRankTC) * E + e] + p.local_rank[a];
-      if (rank < C) { p.final_idx[a] = e; p.slot[a] = rank; }
-      else { p.final_idx[a] = kPendingMark; p.slot[a] = -1; }
-    }
-    __syncthreads();
-    auto has_pending = [&](int t) {
-      for (int j = 0; j < k; ++j) if (p.final_idx[(size_t)t * k + j] == kPendingMark) return true;
-      return false;
-    };
-    int npend = block_compact(N, has_pending, [](int t) { return t; }, p.pend, warp_tot, &s_total);
-    // 3. reroute rounds
-    int round = 0;
-    while (npend > 0) {
-      if (round > E + 1) {               // cannot happen: every round fills an expert or ends
-        set_status(p.status, kDevBadState);
-        break;
-      }
-      for (int e = tid; e < E; e += kPlanThreads) { full_s[e] = fill[e] >= C; prop_cnt[e] = 0; }
-      if (tid == 0) s_any = 0;
-      __syncthreads();
-      for (int c0 = 0; c0 < npend; c0 += kPlanThreads) {
-        for (int i = tid; i < E * 32; i += kPlanThreads) bits[i] = 0;
-        __syncthreads();
-        const int i = tid;
-        const int t = (c0 + i < npend) ? p.pend[c0 + i] : -1;
-        int prop[kMaxTopk];
-        if (t >= 0) {
-          int held[kMaxTopk];
-          for (int j = 0; j < k; ++j) held[j] = p.final_idx[(size_t)t * k + j];
-          for (int j = 0; j < k; ++j) {
-            prop[j] = -1;
-            if (held[j] != kPendingMark) continue;
-            float bp = -1.f;
-            int be = -1;
-            const float* pr = p.probs + (size_t)t * E;
-            for (int e = 0; e < E; ++e) {
-              if (full_s[e]) continue;
-              bool skip = false;
-              for (int jj = 0; jj < k; ++jj) skip |= (held[jj] == e) | (jj < j && prop[jj] == e);
-              if (skip) continue;
-              const float pe = pr[e];
-              if (be < 0 || better(pe, e, bp, be)) { bp = pe; be = e; }
-            }
-            prop[j] = be;
-            if (be < 0) {
-              p.final_idx[(size_t)t * k + j] = -1;          // nothing left: dropped
-            } else {
-              atomicOr(&bits[be * 32 + (i >> 5)], 1u << (i & 31));
-              s_any = 1;
-            }
-          }
-        }
-        __syncthreads();
-        for (int e = tid; e < E; e += kPlanThreads) {
-          int run = 0;
-          for (int w = 0; w < 32; ++w) { pre[e * 32 + w] = run; run += __popc(bits[e * 32 + w]); }
-          chunk_tot[e] = run;
-        }
-        __syncthreads();
-        if (t >= 0) {
-          for (int j = 0; j < k; ++j) {
-            const int e = prop[j];
-            if (e < 0) continue;
-            const int rank = prop_cnt[e] + pre[e * 32 + (i >> 5)] +
-                             __popc(bits[e * 32 + (i >> 5)] & lanemask_lt());
-            const int s = fill[e] + rank;
-            if (s < C) { p.final_idx[(size_t)t * k + j] = e; p.slot[(size_t)t * k + j] = s; }
-          }
-        }
-        __syncthreads();
-        for (int e = tid; e < E; e += kPlanThreads) prop_cnt[e] += chunk_tot[e];
-        __syncthreads();
-      }
-      for (int e = tid; e < E; e += kPlanThreads) fill[e] = min(C, fill[e] + prop_cnt[e]);
-      __syncthreads();
-      if (!s_any) break;
-      npend = block_compact(npend, [&](int q) { return has_pending(p.pend[q]); },
-                            [&](int q) { return p.pend[q]; }, p.pend, warp_tot, &s_total);
-      ++round;
-    }
-    // anything still pending after a bad state is dropped
-    for (int a = tid; a < N * k; a += kPlanThreads)
-      if (p.final_idx[a] == kPendingMark) p.final_idx[a] = -1;
-    __syncthreads();
-  }
-
-  // 4. totals: dropped and rerouted
-  int nd = 0, nr = 0;
-  if (p.cap_mode == 2) {
-    for (int a = tid; a < N * k; a += kPlanThreads) {
-      const int f = p.final_idx[a];
-      nd += (f < 0);
-      nr += (f >= 0 && f != p.topk_idx[a]);
-    }
-  } else {
-    for (int e = tid; e < E; e += kPlanThreads) nd += total[e] - fill[e];
-  }
-  nd = __reduce_add_sync(0xffffffffu, nd);
-  nr = __reduce_add_sync(0xffffffffu, nr);
-  if (lane == 0) warp_tot[tid >> 5] = nd;
-  __syncthreads();
-  if (tid == 0) { int s = 0; for (int w = 0; w < kPlanThreads / 32; ++w) s += warp_tot[w]; s_total = s; }
-  __syncthreads();
-  const int n_dropped = s_total;
-  __syncthreads();
-  if (lane == 0) warp_tot[tid >> 5] = nr;
-  __syncthreads();
-  if (tid == 0) {
-    int s = 0;
-    for (int w = 0; w < kPlanThreads / 32; ++w) s += warp_tot[w];
+// Segment layout, counts and drop/reroute totals from the final per-expert
+// fill levels; perm = -1 on the padding rows.  Executed by one whole CTA.
+__device__ void write_layout(const DispatchParams& p, const int* fill, int n_dropped,
+                             int n_rerouted) {
+  const int E = p.E, S = p.S, N = p.N;
+  if (threadIdx.x == 0) {
     if (p.n_dropped) *p.n_dropped = n_dropped;
-    if (p.n_rerouted) *p.n_rerouted = s;
-    // 5. segment layout: routed experts, then shared experts
+    if (p.n_rerouted) *p.n_rerouted = n_rerouted;
     int row = 0;
     for (int e = 0; e < E; ++e) {
       p.offsets[e] = row;
       row += (fill[e] + kAlign - 1) / kAlign * kAlign;
     }
     const int nseg = (N + kAlign - 1) / kAlign * kAlign;
-    for (int s2 = 0; s2 < S; ++s2) { p.offsets[E + s2] = row; row += nseg; }
+    for (int s = 0; s < S; ++s) { p.offsets[E + s] = row; row += nseg; }
     p.offsets[E + S] = row;
   }
-  for (int e = tid; e < E; e += kPlanThreads) if (p.counts) p.counts[e] = fill[e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) if (p.counts) p.counts[e] = fill[e];
   __syncthreads();
-  // 6. perm = -1 on the padding rows of routed segments (one warp per expert)
-  for (int e = tid >> 5; e < E; e += kPlanThreads / 32) {
+  const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  for (int e = threadIdx.x >> 5; e < E; e += nw) {
     const int r0 = p.offsets[e] + fill[e];
     const int r1 = p.offsets[e + 1];
     for (int r = r0 + lane; r < r1; r += 32) p.perm[r] = -1;
+  }
+}
+
+__global__ void __launch_bounds__(kPlanThreads) dispatch_plan_kernel(DispatchParams p) {
+  const int E = p.E, k = p.k, N = p.N, C = p.C;
+  __shared__ int fill[kMaxExperts], total[kMaxExperts];
+  __shared__ int warp_tot[kPlanThreads / 32];
+  __shared__ int s_total;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // per-expert exclusive scan over token chunks (a warp per expert)
+  for (int e = warp; e < E; e += kPlanThreads / 32) {
+    const int run = warp_exclusive_scan_column(p.chunk_cnt, p.n_chunks, E, e, lane);
+    if (lane == 0) { total[e] = run; fill[e] = min(run, C); }
+  }
+  __syncthreads();
+
+  if (p.cap_mode != 2) {
+    int nd = 0;
+    for (int e = tid; e < E; e += kPlanThreads) nd += total[e] - fill[e];
+    nd = __reduce_add_sync(0xffffffffu, nd);
+    if (lane == 0) warp_tot[warp] = nd;
+    __syncthreads();
+    if (tid == 0) { int s = 0; for (int w = 0; w < kPlanThreads / 32; ++w) s += warp_tot[w]; s_total = s; }
+    __syncthreads();
+    write_layout(p, fill, s_total, 0);
+    return;
+  }
+
+  // reroute: primary pass keeps rank < C and marks the rest pending
+  for (int a = tid; a < N * k; a += kPlanThreads) {
+    const int t = a / k;
+    const int e = p.topk_idx[a];
+    if (!valid_expert(e, E)) { p.final_idx[a] = -1; p.slot[a] = -1; continue; }
+    const int rank = p.chunk_cnt[(size_t)(t / kRankTC) * E + e] + p.local_rank[a];
+    if (rank < C) { p.final_idx[a] = e; p.slot[a] = rank; }
+    else { p.final_idx[a] = kPendingMark; p.slot[a] = -1; }
+  }
+  __syncthreads();
+  // tokens with a pending slot, in ascending order (block-wide compaction)
+  int base = 0;
+  for (int c0 = 0; c0 < N; c0 += kPlanThreads) {
+    const int t = c0 + tid;
+    bool f = false;
+    if (t < N)
+      for (int j = 0; j < k; ++j) f |= p.final_idx[(size_t)t * k + j] == kPendingMark;
+    const uint32_t bal = __ballot_sync(0xffffffffu, f);
+    if (lane == 0) warp_tot[warp] = __popc(bal);
+    __syncthreads();
+    if (tid == 0) {
+      int run = 0;
+      for (int w = 0; w < kPlanThreads / 32; ++w) { const int c = warp_tot[w]; warp_tot[w] = run; run += c; }
+      s_total = run;
+    }
+    __syncthreads();
+    if (f) p.pend[base + warp_tot[warp] + __popc(bal & lanemask_lt())] = t;
+    base += s_total;
+    __syncthreads();
+  }
+  int kept = 0;
+  for (int e = tid; e < E; e += kPlanThreads) { p.rr->fill[0][e] = fill[e]; kept += fill[e]; }
+  kept = __reduce_add_sync(0xffffffffu, kept);
+  if (lane == 0) warp_tot[warp] = kept;
+  __syncthreads();
+  if (tid == 0) {
+    int s = 0;
+    for (int w = 0; w < kPlanThreads / 32; ++w) s += warp_tot[w];
+    p.rr->primary_kept = s;
+    p.rr->n_pending = base;
+    p.rr->bar_count = 0;
+    p.rr->bar_gen = 0;
+  }
+  for (int r = tid; r < kMaxRounds; r += kPlanThreads) { p.rr->any_prop[r] = 0; p.rr->left[r] = 0; }
+}
+
+// Grid-wide barrier for a cooperative launch (all CTAs co-resident).  Bounded:
+// after kWaitLimitNs the waiting CTA records kDevTimeout and gives up.
+__device__ void grid_barrier(RerouteState* rr, int* status) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile unsigned* gen = &rr->bar_gen;
+    const unsigned g = *gen;
+    __threadfence();
+    const unsigned arrived = atomicAdd(&rr->bar_count, 1u);
+    if (arrived == gridDim.x - 1) {
+      atomicExch(&rr->bar_count, 0u);
+      __threadfence();
+      atomicAdd(&rr->bar_gen, 1u);
+    } else {
+      const uint64_t t0 = globaltimer_ns();
+      while (*gen == g) {
+        __nanosleep(64);
+        if (globaltimer_ns() - t0 > kWaitLimitNs) { set_status(status, kDevTimeout); break; }
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  __threadfence();
+}
+
+__global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchParams p) {
+  const int E = p.E, k = p.k, C = p.C;
+  RerouteState* rr = p.rr;
+  __shared__ uint32_t bits[kMaxExperts * kRrWords];
+  __shared__ unsigned char full_s[kMaxExperts];
+  __shared__ int fill_s[kMaxExperts];
+  const int tid = threadIdx.x;
+  const int P = __ldcg(&rr->n_pending);
+  const int nch = (P + kRrThreads - 1) / kRrThreads;
+  int round = 0;
+  int cur = 0;                                   // fill[cur] = levels at the start of the round
+  while (P > 0) {
+    if (round >= kMaxRounds || round > E + 1) { set_status(p.status, kDevBadState); break; }
+    // ---- phase A: proposals and per-chunk bitmap ranks
+    for (int e = tid; e < E; e += kRrThreads) full_s[e] = __ldcg(&rr->fill[cur][e]) >= C;
+    __syncthreads();
+    for (int c = blockIdx.x; c < nch; c += gridDim.x) {
+      for (int i = tid; i < E * kRrWords; i += kRrThreads) bits[i] = 0;
+      __syncthreads();
+      const int idx = c * kRrThreads + tid;
+      const int t = idx < P ? p.pend[idx] : -1;
+      int prop[kMaxTopk];
+      bool any = false;
+      if (t >= 0) {
+        int held[kMaxTopk];
+        for (int j = 0; j < k; ++j) held[j] = p.final_idx[(size_t)t * k + j];
+        const float* pr = p.probs + (size_t)t * E;
+        for (int j = 0; j < k; ++j) {
+          prop[j] = -1;
+          if (held[j] != kPendingMark) continue;
+          float bp = -1.f;
+          int be = -1;
+          for (int e0 = 0; e0 < E; e0 += 8) {
+            float pv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) pv[u] = (e0 + u < E) ? pr[e0 + u] : -1.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int e = e0 + u;
+              if (e >= E || full_s[e]) continue;
+              bool skip = false;
+              for (int jj = 0; jj < k; ++jj) skip |= (held[jj] == e) | (jj < j && prop[jj] == e);
+              if (skip) continue;
+              if (be < 0 || better(pv[u], e, bp, be)) { bp = pv[u]; be = e; }
+            }
+          }
+          prop[j] = be;
+          if (be < 0) {
+            p.final_idx[(size_t)t * k + j] = -1;          // nothing left: dropped
+          } else {
+            atomicOr(&bits[be * kRrWords + (tid >> 5)], 1u << (tid & 31));
+            any = true;
+          }
+        }
+      }
+      if (__syncthreads_or(any) && tid == 0) atomicExch(&rr->any_prop[round], 1);
+      if (t >= 0) {
+        for (int j = 0; j < k; ++j) {
+          const int e = prop[j];
+          int r = -1;
+          if (e >= 0) {
+            r = 0;
+            for (int w = 0; w < (tid >> 5); ++w) r += __popc(bits[e * kRrWords + w]);
+            r += __popc(bits[e * kRrWords + (tid >> 5)] & lanemask_lt());
+          }
+          p.rr_prop[(size_t)idx * k + j] = e;
+          p.rr_rank[(size_t)idx * k + j] = r;
+        }
+      }
+      for (int e = tid; e < E; e += kRrThreads) {
+        int n = 0;
+        for (int w = 0; w < kRrWords; ++w) n += __popc(bits[e * kRrWords + w]);
+        p.rr_chunk[(size_t)c * E + e] = n;
+      }
+      __syncthreads();
+    }
+    grid_barrier(rr, p.status);
+    // ---- phase B: per-expert exclusive scan over chunks (a warp per expert),
+    //      next fill levels
+    {
+      const int lane = tid & 31;
+      const int nwarps = gridDim.x * (kRrThreads / 32);
+      for (int e = blockIdx.x * (kRrThreads / 32) + (tid >> 5); e < E; e += nwarps) {
+        const int carry = warp_exclusive_scan_column(p.rr_chunk, nch, E, e, lane);
+        if (lane == 0) rr->fill[cur ^ 1][e] = min(C, __ldcg(&rr->fill[cur][e]) + carry);
+      }
+    }
+    grid_barrier(rr, p.status);
+    // ---- phase C: acceptance in token order while the expert has room
+    for (int e = tid; e < E; e += kRrThreads) fill_s[e] = __ldcg(&rr->fill[cur][e]);
+    __syncthreads();
+    int left = 0;
+    for (int c = blockIdx.x; c < nch; c += gridDim.x) {
+      const int idx = c * kRrThreads + tid;
+      if (idx >= P) continue;
+      const int t = p.pend[idx];
+      for (int j = 0; j < k; ++j) {
+        const int e = p.rr_prop[(size_t)idx * k + j];
+        if (e < 0) continue;
+        const int s = fill_s[e] + __ldcg(&p.rr_chunk[(size_t)c * E + e]) + p.rr_rank[(size_t)idx * k + j];
+        if (s < C) { p.final_idx[(size_t)t * k + j] = e; p.slot[(size_t)t * k + j] = s; }
+        else ++left;
+      }
+    }
+    if (__syncthreads_or(left > 0) && tid == 0) atomicExch(&rr->left[round], 1);
+    grid_barrier(rr, p.status);
+    cur ^= 1;
+    const bool stop = !__ldcg(&rr->any_prop[round]) || !__ldcg(&rr->left[round]);
+    ++round;
+    if (stop) break;
+  }
+  // ---- layout from the final fill levels (CTA 0)
+  if (blockIdx.x == 0) {
+    __syncthreads();
+    for (int e = tid; e < E; e += kRrThreads) fill_s[e] = __ldcg(&rr->fill[cur][e]);
+    __syncthreads();
+    __shared__ int s_kept;
+    if (tid == 0) {
+      int kept = 0;
+      for (int e = 0; e < E; ++e) kept += fill_s[e];
+      s_kept = kept;
+    }
+    __syncthreads();
+    write_layout(p, fill_s, p.N * k - s_kept, s_kept - __ldcg(&rr->primary_kept));
   }
 }
 
@@ -268,9 +360,10 @@ __global__ void __launch_bounds__(128) dispatch_scatter_kernel(DispatchParams p)
     if (p.cap_mode == 2) {
       f = p.final_idx[a];
       sl = p.slot[a];
+      if (f < 0) { f = -1; p.final_idx[a] = -1; }
     } else {
       const int e = p.topk_idx[a];
-      if (e >= 0 && e < E) {
+      if (valid_expert(e, E)) {
         sl = p.chunk_cnt[(size_t)(t / kRankTC) * E + e] + p.local_rank[a];
         f = (sl < p.C) ? e : -1;
       } else {
@@ -299,18 +392,37 @@ __global__ void __launch_bounds__(128) dispatch_scatter_kernel(DispatchParams p)
 
 }  // namespace
 
+size_t reroute_scratch_ints(int N, int k, int E) {
+  const size_t chunks = (size_t)(N + kRrThreads - 1) / kRrThreads;
+  return 2 * (size_t)N * k + chunks * E;
+}
+
 cudaError_t launch_dispatch(const DispatchParams& p, bool bf16, cudaStream_t s) {
   const int W = kRankTC / 32;
   dispatch_rank_kernel<<<p.n_chunks, kRankTC, sizeof(uint32_t) * p.E * W, s>>>(p);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const size_t plan_smem = (size_t)p.E * 32 * 8;
-  err = cudaFuncSetAttribute(dispatch_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)plan_smem);
-  if (err != cudaSuccess) return err;
-  dispatch_plan_kernel<<<1, kPlanThreads, plan_smem, s>>>(p);
+  dispatch_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  if (p.cap_mode == 2) {
+    int dev = 0, sms = 0, per_sm = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return err;
+    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_reroute_kernel,
+                                                             kRrThreads, 0)) != cudaSuccess)
+      return err;
+    const int max_chunks = (p.N + kRrThreads - 1) / kRrThreads;
+    int grid = sms * (per_sm < 2 ? per_sm : 2);
+    if (grid > max_chunks) grid = max_chunks;
+    if (grid < 1) grid = 1;
+    DispatchParams q = p;
+    void* args[] = {&q};
+    err = cudaLaunchCooperativeKernel((const void*)dispatch_reroute_kernel, dim3(grid),
+                                      dim3(kRrThreads), args, 0, s);
+    if (err != cudaSuccess) return err;
+  }
   if (bf16) dispatch_scatter_kernel<__nv_bfloat16><<<p.N, 128, 0, s>>>(p);
   else dispatch_scatter_kernel<float><<<p.N, 128, 0, s>>>(p);
   return cudaGetLastError();

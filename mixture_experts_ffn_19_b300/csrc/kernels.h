@@ -21,9 +21,21 @@ struct RouteParams {
   int32_t* topk_idx;         // [N, k]
   float* topk_w;             // [N, k]
   float* probs;              // [N, E] or null
-  float* psum_part;          // [blocks, E]
-  int32_t* picks_part;       // [blocks, E]
+  float* part;               // [ks, N, E] partial logits (one per K slice)
+  float* psum_part;          // [route_finish_blocks(N), E]
+  int32_t* picks_part;       // [route_finish_blocks(N), E]
+  int* status;
 };
+
+// Split of the router contraction over K: ks slices of k_slice (a multiple of 64).
+struct RouteSplit {
+  int ks, k_slice;
+};
+RouteSplit route_split(int N, int d, bool bf16);
+int route_finish_blocks(int N);
+cudaError_t launch_route_logits_tc(const RouteSplit& s, const void* x, const void* w_router,
+                                   int N, int E, int d, float* part, int* status,
+                                   cudaStream_t stream);
 
 struct RouteStatsParams {
   const float* psum_part;
@@ -33,6 +45,18 @@ struct RouteStatsParams {
   float* mean_prob;          // nullable
   float* l_bal;              // nullable
 };
+
+constexpr int kMaxRounds = 260;   // reroute rounds never exceed E + 1 <= 257
+
+// Device state shared by the CTAs of the cooperative reroute launch.
+struct RerouteState {
+  int fill[2][kMaxExperts];      // per-expert fill levels, double-buffered by round
+  int any_prop[kMaxRounds];      // round r made at least one proposal
+  int left[kMaxRounds];          // round r left a proposal rejected
+  int primary_kept, n_pending;
+  unsigned bar_count, bar_gen;   // grid barrier
+};
+size_t reroute_scratch_ints(int N, int k, int E);
 
 struct DispatchParams {
   int N, E, k, S, d, cap_mode, C;
@@ -49,6 +73,10 @@ struct DispatchParams {
   int32_t* perm;             // [max_rows]
   void* x_perm;              // [max_rows, d]
   int32_t* pend;             // [N] scratch (pending token list)
+  RerouteState* rr;          // reroute state (workspace)
+  int32_t* rr_prop;          // [N, k] proposals of the round
+  int32_t* rr_rank;          // [N, k] rank of each proposal inside its chunk
+  int32_t* rr_chunk;         // [ceil(N/128), E] per-chunk proposal counts, then bases
   int32_t* counts;           // [E] nullable
   int32_t* n_dropped;        // nullable
   int32_t* n_rerouted;       // nullable

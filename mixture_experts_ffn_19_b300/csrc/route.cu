@@ -1,16 +1,15 @@
-// Router: logits z = x W_r^T (+ b), fp32 softmax, top-k with renormalised
-// gates, and the per-CTA partial sums of the load-balance statistics.
+// Router: partial logits (fp32 layers: CUDA-core contraction here; bf16 layers:
+// tensor cores, route_tc.cu), then a warp-per-token finish: sum of the K-slice
+// partials, router bias, fp32 softmax, top-k with renormalised gates, and the
+// per-CTA partial sums of the load-balance statistics.
 //
 // «为什么MoE有效？稀疏激活的数学直觉与工程实践» §2.2 (router = bias-free linear
 // map, softmax, torch.topk, renormalise); «DeepSeek-V2 ...» summary §2.2
 // (expert_bias added to the logits before the softmax; load_balance_loss).
 //
-// One CTA owns 32 tokens.  The contraction is tiled through shared memory
-// (64-wide K chunks, fp32 FMA, each K chunk summed separately and folded into
-// the running sum with Kahan compensation so the logits stay within ~1e-7 of
-// the exact value: top-k decisions then only differ from an exact evaluation
-// on genuine near-ties).  The epilogue is warp-per-token: softmax with warp
-// shuffles, then k rounds of a shuffle arg-max (ties to the lower expert).
+// The K-slice partials are summed in double in slice order, so the logits are
+// within ~1e-7 of the exact value and deterministic; top-k is k rounds of a
+// warp-shuffle arg-max (higher probability first, ties to the lower index).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -18,45 +17,35 @@ namespace moe {
 
 namespace {
 
-constexpr int kTM = kRouteTM;   // tokens per CTA
-constexpr int kKC = 64;         // K chunk
+constexpr int kTM = kRouteTM;   // tokens per CUDA-core logits CTA
+constexpr int kKC = 64;         // K chunk staged through shared memory
 constexpr int kXS = kKC + 4;    // padded smem row (floats), 16-byte aligned rows
 constexpr int kThreads = 256;
+constexpr int kFinishTokens = 64;   // tokens per finish CTA (8 warps x 8)
 
-template <typename T>
-__device__ __forceinline__ void load8(const T* src, float (&v)[8]);
-
-template <>
-__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* src, float (&v)[8]) {
-  const uint4 u = *reinterpret_cast<const uint4*>(src);
-  v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
-  v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z); v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
-}
-template <>
-__device__ __forceinline__ void load8<float>(const float* src, float (&v)[8]) {
+__device__ __forceinline__ void load8f(const float* src, float (&v)[8]) {
   const float4 a = reinterpret_cast<const float4*>(src)[0];
   const float4 b = reinterpret_cast<const float4*>(src)[1];
   v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-// EJ = experts per thread column group = ceil(E / 32).
-template <typename T, int EJ>
-__global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
+// fp32 partial logits on the CUDA cores (no TF32: 1e-4 accuracy is required).
+// Grid (ceil(N/32), ks); EJ = ceil(E/32).  Each K chunk is summed separately and
+// folded into the running sum with Kahan compensation.
+template <int EJ>
+__global__ void __launch_bounds__(kThreads) route_logits_simt(RouteParams p, RouteSplit sp) {
   extern __shared__ __align__(16) float sm[];
-  const int E = p.E, d = p.d, k = p.k, N = p.N;
-  const int EP = EJ * 32;                        // padded expert rows
+  const int E = p.E, d = p.d, N = p.N;
+  const int EP = EJ * 32;
   float* xs = sm;                                // [kTM][kXS]
   float* ws = xs + kTM * kXS;                    // [EP][kXS]
-  float* lg = ws + EP * kXS;                     // [kTM][EP+1] logits, then probabilities
-  int* picks_s = reinterpret_cast<int*>(lg + kTM * (EP + 1));   // [EP]
-
   const int tid = threadIdx.x;
   const int t0 = blockIdx.x * kTM;
-  const T* x = static_cast<const T*>(p.x);
-  const T* wr = static_cast<const T*>(p.w_router);
-
-  const int tx = tid & 7;      // tokens tx, tx+8, tx+16, tx+24
-  const int ty = tid >> 3;     // experts ty, ty+32, ...
+  const int ks = blockIdx.y;
+  const int k_begin = ks * sp.k_slice, k_end = min(d, k_begin + sp.k_slice);
+  const float* x = static_cast<const float*>(p.x);
+  const float* wr = static_cast<const float*>(p.w_router);
+  const int tx = tid & 7, ty = tid >> 3;
 
   float sum[4][EJ], cmp[4][EJ];
 #pragma unroll
@@ -64,19 +53,18 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
 #pragma unroll
     for (int j = 0; j < EJ; ++j) sum[i][j] = cmp[i][j] = 0.f;
 
-  for (int k0 = 0; k0 < d; k0 += kKC) {
-    // stage x tile [kTM][kKC] and W tile [EP][kKC] as fp32 (zero outside)
+  for (int k0 = k_begin; k0 < k_end; k0 += kKC) {
     for (int v = tid; v < kTM * (kKC / 8); v += kThreads) {
       const int r = v / (kKC / 8), c = (v % (kKC / 8)) * 8;
       float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      if (t0 + r < N && k0 + c < d) load8<T>(x + (size_t)(t0 + r) * d + k0 + c, f);
+      if (t0 + r < N && k0 + c < k_end) load8f(x + (size_t)(t0 + r) * d + k0 + c, f);
 #pragma unroll
       for (int q = 0; q < 8; ++q) xs[r * kXS + c + q] = f[q];
     }
     for (int v = tid; v < EP * (kKC / 8); v += kThreads) {
       const int r = v / (kKC / 8), c = (v % (kKC / 8)) * 8;
       float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      if (r < E && k0 + c < d) load8<T>(wr + (size_t)r * d + k0 + c, f);
+      if (r < E && k0 + c < k_end) load8f(wr + (size_t)r * d + k0 + c, f);
 #pragma unroll
       for (int q = 0; q < 8; ++q) ws[r * kXS + c + q] = f[q];
     }
@@ -107,7 +95,6 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
           acc[i][j] = a;
         }
     }
-    // fold the chunk into the running sum with Kahan compensation
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -119,33 +106,47 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
       }
     __syncthreads();
   }
-
-  // logits (+ bias) -> smem
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + tx + 8 * i;
+    if (t >= N) continue;
 #pragma unroll
     for (int j = 0; j < EJ; ++j) {
       const int e = ty + 32 * j;
-      if (e < E) lg[(tx + 8 * i) * (EP + 1) + e] = sum[i][j] + (p.bias ? p.bias[e] : 0.f);
+      if (e < E) p.part[((size_t)ks * N + t) * E + e] = sum[i][j];
     }
+  }
+}
+
+// Warp per token: logits from the partials, bias, softmax, top-k, gates.
+template <int EJ>
+__global__ void __launch_bounds__(kThreads) route_finish_kernel(RouteParams p, RouteSplit sp) {
+  constexpr int EP = EJ * 32;
+  __shared__ float psum_w[kThreads / 32][EP];
+  __shared__ int picks_s[EP];
+  const int E = p.E, N = p.N, k = p.k;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int e = tid; e < EP; e += kThreads) picks_s[e] = 0;
   __syncthreads();
-
-  // warp-per-token epilogue
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int r = warp; r < kTM; r += kThreads / 32) {
-    const int t = t0 + r;
-    float* row = lg + r * (EP + 1);
-    if (t >= N) {
-      for (int c = 0; c < EJ; ++c) if (lane + 32 * c < E) row[lane + 32 * c] = 0.f;
-      continue;
-    }
+  float psum[EJ];
+#pragma unroll
+  for (int c = 0; c < EJ; ++c) psum[c] = 0.f;
+  const int tpw = kFinishTokens / (kThreads / 32);
+  for (int i = 0; i < tpw; ++i) {
+    const int t = blockIdx.x * kFinishTokens + warp * tpw + i;
+    if (t >= N) break;
     float v[EJ];
     float m = -INFINITY;
 #pragma unroll
     for (int c = 0; c < EJ; ++c) {
       const int e = lane + 32 * c;
-      v[c] = (e < E) ? row[e] : -INFINITY;
+      if (e < E) {
+        double z = 0.0;
+        for (int s = 0; s < sp.ks; ++s) z += (double)p.part[((size_t)s * N + t) * E + e];
+        v[c] = (float)z + (p.bias ? p.bias[e] : 0.f);
+      } else {
+        v[c] = -INFINITY;
+      }
       m = fmaxf(m, v[c]);
     }
     m = warp_max(m);
@@ -161,15 +162,13 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
       const int e = lane + 32 * c;
       v[c] = v[c] / s;
       if (e < E) {
-        row[e] = v[c];
+        psum[c] += v[c];
         if (p.probs) p.probs[(size_t)t * E + e] = v[c];
       }
     }
-    // top-k: k rounds of arg-max (higher p, then lower index)
     uint32_t taken = 0;
-    float sel_p[8];
-    int sel_e[8];
-    float ksum = 0.f;
+    float ksum = 0.f, my_p = 0.f;
+    int my_e = 0;
     for (int q = 0; q < k; ++q) {
       float bp = -1.f;
       int be = 0x7fffffff;
@@ -185,39 +184,48 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
         if (better(op, oe, bp, be)) { bp = op; be = oe; }
       }
       if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      sel_p[q] = bp;
-      sel_e[q] = be;
+      if (q == lane) { my_p = bp; my_e = be; }
       ksum += bp;
     }
     if (lane < k) {
-      float mp = 0.f;
-      int me = 0;
-      for (int q = 0; q < k; ++q) if (q == lane) { mp = sel_p[q]; me = sel_e[q]; }
-      p.topk_idx[(size_t)t * k + lane] = me;
-      p.topk_w[(size_t)t * k + lane] = mp / ksum;
-      atomicAdd(&picks_s[me], 1);
+      p.topk_idx[(size_t)t * k + lane] = my_e;
+      p.topk_w[(size_t)t * k + lane] = my_p / ksum;
+      atomicAdd(&picks_s[my_e], 1);
     }
   }
+#pragma unroll
+  for (int c = 0; c < EJ; ++c) psum_w[warp][lane + 32 * c] = psum[c];
   __syncthreads();
-  // per-CTA partial statistics, summed in token order (deterministic)
+  // per-CTA partial statistics, warps summed in order (deterministic)
   for (int e = tid; e < E; e += kThreads) {
     float acc = 0.f;
-    for (int r = 0; r < kTM; ++r) acc += lg[r * (EP + 1) + e];
+    for (int w = 0; w < kThreads / 32; ++w) acc += psum_w[w][e];
     p.psum_part[(size_t)blockIdx.x * E + e] = acc;
     p.picks_part[(size_t)blockIdx.x * E + e] = picks_s[e];
   }
 }
 
-__global__ void __launch_bounds__(256) route_stats_kernel(RouteStatsParams p) {
-  __shared__ double contrib[256];
-  const int e = threadIdx.x;
+// expert_freq, mean_prob and L_bal from the per-CTA partials: 4 threads per
+// expert each sum a fixed stride of rows in double, combined in a fixed order.
+__global__ void __launch_bounds__(1024) route_stats_kernel(RouteStatsParams p) {
+  __shared__ double part_s[kMaxExperts][4];
+  __shared__ long long pick_s[kMaxExperts][4];
+  __shared__ double contrib[kMaxExperts];
+  const int e = threadIdx.x >> 2, q = threadIdx.x & 3;
   if (e < p.E) {
     double sp = 0.0;
     long long pk = 0;
-    for (int b = 0; b < p.blocks; ++b) {
+    for (int b = q; b < p.blocks; b += 4) {
       sp += (double)p.psum_part[(size_t)b * p.E + e];
       pk += p.picks_part[(size_t)b * p.E + e];
     }
+    part_s[e][q] = sp;
+    pick_s[e][q] = pk;
+  }
+  __syncthreads();
+  if (e < p.E && q == 0) {
+    const double sp = ((part_s[e][0] + part_s[e][1]) + part_s[e][2]) + part_s[e][3];
+    const long long pk = pick_s[e][0] + pick_s[e][1] + pick_s[e][2] + pick_s[e][3];
     const double mean = sp / (double)p.N;
     const double freq = (double)pk / ((double)p.N * (double)p.k);
     if (p.mean_prob) p.mean_prob[e] = (float)mean;
@@ -232,42 +240,65 @@ __global__ void __launch_bounds__(256) route_stats_kernel(RouteStatsParams p) {
   }
 }
 
-template <typename T, int EJ>
-cudaError_t launch_route_t(const RouteParams& p, cudaStream_t s) {
-  const int EP = EJ * 32;
-  const size_t smem = sizeof(float) * ((size_t)kTM * kXS + (size_t)EP * kXS +
-                                       (size_t)kTM * (EP + 1)) + sizeof(int) * EP;
-  auto kern = route_kernel<T, EJ>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+template <int EJ>
+cudaError_t launch_simt_t(const RouteParams& p, const RouteSplit& sp, cudaStream_t s) {
+  const size_t smem = sizeof(float) * ((size_t)kTM * kXS + (size_t)EJ * 32 * kXS);
+  auto kern = route_logits_simt<EJ>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  const int blocks = (p.N + kTM - 1) / kTM;
-  kern<<<blocks, kThreads, smem, s>>>(p);
+  kern<<<dim3((p.N + kTM - 1) / kTM, sp.ks), kThreads, smem, s>>>(p, sp);
   return cudaGetLastError();
 }
 
-template <typename T>
-cudaError_t launch_route_dt(const RouteParams& p, cudaStream_t s) {
-  switch ((p.E + 31) / 32) {
-    case 1: return launch_route_t<T, 1>(p, s);
-    case 2: return launch_route_t<T, 2>(p, s);
-    case 3: return launch_route_t<T, 3>(p, s);
-    case 4: return launch_route_t<T, 4>(p, s);
-    case 5: return launch_route_t<T, 5>(p, s);
-    case 6: return launch_route_t<T, 6>(p, s);
-    case 7: return launch_route_t<T, 7>(p, s);
-    default: return launch_route_t<T, 8>(p, s);
-  }
+template <int EJ>
+cudaError_t launch_finish_t(const RouteParams& p, const RouteSplit& sp, cudaStream_t s) {
+  route_finish_kernel<EJ><<<route_finish_blocks(p.N), kThreads, 0, s>>>(p, sp);
+  return cudaGetLastError();
 }
+
+#define MOE_EJ_SWITCH(E, F, ...)                  \
+  switch (((E) + 31) / 32) {                      \
+    case 1: return F<1>(__VA_ARGS__);             \
+    case 2: return F<2>(__VA_ARGS__);             \
+    case 3: return F<3>(__VA_ARGS__);             \
+    case 4: return F<4>(__VA_ARGS__);             \
+    case 5: return F<5>(__VA_ARGS__);             \
+    case 6: return F<6>(__VA_ARGS__);             \
+    case 7: return F<7>(__VA_ARGS__);             \
+    default: return F<8>(__VA_ARGS__);            \
+  }
 
 }  // namespace
 
+int route_finish_blocks(int N) { return (N + kFinishTokens - 1) / kFinishTokens; }
+
+RouteSplit route_split(int N, int d, bool bf16) {
+  const int tile = bf16 ? 128 : kTM;
+  const int tiles = (N + tile - 1) / tile;
+  const int kblocks = (d + 63) / 64;
+  int ks = (2 * 148 + tiles - 1) / tiles;
+  ks = ks < 1 ? 1 : (ks > kblocks ? kblocks : ks);
+  const int k_slice = (kblocks + ks - 1) / ks * 64;
+  RouteSplit r;
+  r.k_slice = k_slice;
+  r.ks = (d + k_slice - 1) / k_slice;
+  return r;
+}
+
 cudaError_t launch_route(const RouteParams& p, bool bf16, cudaStream_t s) {
-  return bf16 ? launch_route_dt<__nv_bfloat16>(p, s) : launch_route_dt<float>(p, s);
+  const RouteSplit sp = route_split(p.N, p.d, bf16);
+  cudaError_t err;
+  if (bf16) {
+    err = launch_route_logits_tc(sp, p.x, p.w_router, p.N, p.E, p.d, p.part, p.status, s);
+  } else {
+    err = [&]() -> cudaError_t { MOE_EJ_SWITCH(p.E, launch_simt_t, p, sp, s) }();
+  }
+  if (err != cudaSuccess) return err;
+  MOE_EJ_SWITCH(p.E, launch_finish_t, p, sp, s)
 }
 
 cudaError_t launch_route_stats(const RouteStatsParams& p, cudaStream_t s) {
-  route_stats_kernel<<<1, 256, 0, s>>>(p);
+  route_stats_kernel<<<1, 1024, 0, s>>>(p);
   return cudaGetLastError();
 }
 
