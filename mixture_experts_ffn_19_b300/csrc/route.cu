@@ -274,7 +274,7 @@ int route_finish_blocks(int N) { return (N + kFinishTokens - 1) / kFinishTokens;
 
 RouteSplit route_split(int N, int d, bool bf16) {
   const int tile = bf16 ? 128 : kTM;
-  const int tiles = (N + tile - 1) / tile;
+  const int tiles = N > 0 ? (N + tile - 1) / tile : 1;
   const int kblocks = (d + 63) / 64;
   int ks = (2 * 148 + tiles - 1) / tiles;
   ks = ks < 1 ? 1 : (ks > kblocks ? kblocks : ks);

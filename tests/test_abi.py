@@ -91,3 +91,12 @@ def test_null_arguments_are_rejected_before_any_launch(lib):
     st = lib.moe_combine(ctypes.byref(c), None, None, None, None, None, None, None)
     assert st == moe.MOE_ERR_INVALID_ARG
     assert moe.status_string(moe.MOE_ERR_WORKSPACE) == "workspace too small"
+
+
+def test_zero_tokens_and_tiny_shapes_size_without_error(lib):
+    for n in (0, 1, 127, 129):
+        c = moe.make_config(n, 64, 4, 2, 64, n_shared=1, cap_mode=moe.MOE_CAP_REROUTE, alpha=1.0)
+        assert moe.moe_validate_config(c) == moe.MOE_OK
+        assert moe.moe_workspace_size(c) > 0
+    c = moe.make_config(0, 128, 8, 2, 256, act=moe.MOE_ACT_GELU, dtype=moe.MOE_F32, has_ffn_bias=True)
+    assert moe.moe_workspace_size(c) > 0
