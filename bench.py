@@ -51,12 +51,64 @@ def peaks():
                 "source": "fallback"}
 
 
+class _Nvml:
+    """Minimal read-only NVML binding over ctypes (libnvidia-ml ships with the driver)."""
+
+    CLOCK_SM = 1
+
+    def __init__(self):
+        import ctypes
+        self.c = ctypes
+        lib = None
+        for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if lib is None:
+            raise RuntimeError("libnvidia-ml not found")
+        self.lib = lib
+        self._ok(lib.nvmlInit_v2())
+
+    def _ok(self, rc):
+        if rc != 0:
+            raise RuntimeError(f"NVML error {rc}")
+
+    def handle(self, torch_device):
+        import torch
+        c = self.c
+        h = c.c_void_p()
+        props = torch.cuda.get_device_properties(torch_device)
+        bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+        if self.lib.nvmlDeviceGetHandleByPciBusId_v2(c.c_char_p(bus.encode()), c.byref(h)) != 0:
+            self._ok(self.lib.nvmlDeviceGetHandleByIndex_v2(c.c_uint(0), c.byref(h)))
+        return h
+
+    def clock(self, h):
+        v = self.c.c_uint()
+        self._ok(self.lib.nvmlDeviceGetClockInfo(h, self.c.c_int(self.CLOCK_SM), self.c.byref(v)))
+        return v.value
+
+    def max_clock(self, h):
+        v = self.c.c_uint()
+        self._ok(self.lib.nvmlDeviceGetMaxClockInfo(h, self.c.c_int(self.CLOCK_SM), self.c.byref(v)))
+        return v.value
+
+    def reasons(self, h):
+        v = self.c.c_ulonglong()
+        f = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self._ok(f(h, self.c.byref(v)))
+        return v.value
+
+
 class ClockSampler:
     """SM clock and clock-event (throttle) reasons sampled through NVML every
     10 ms while the timed region runs (read-only queries)."""
 
-    REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
-               "sw_power_cap": 0x4}
+    REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+               "hw_thermal_slowdown": 0x40}
 
     def __init__(self, torch_device):
         self.dev = torch_device
@@ -64,36 +116,13 @@ class ClockSampler:
         self.reasons = set()
         self.max_mhz = None
         self.stop = threading.Event()
-        self.handle = None
-
-    def _handle(self):
-        import pynvml
-        pynvml.nvmlInit()
-        import torch
-        props = torch.cuda.get_device_properties(self.dev)
-        bus = getattr(props, "pci_bus_id", None)
-        if bus is not None:
-            dom = getattr(props, "pci_domain_id", 0)
-            devid = getattr(props, "pci_device_id", 0)
-            try:
-                return pynvml.nvmlDeviceGetHandleByPciBusId(f"{dom:08x}:{bus:02x}:{devid:02x}.0")
-            except Exception:
-                pass
-        try:
-            return pynvml.nvmlDeviceGetHandleByUUID("GPU-" + str(props.uuid))
-        except Exception:
-            pass
-        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
-        idx = int(vis.split(",")[self.dev.index or 0]) if vis and vis.split(",")[0].isdigit() \
-            else (self.dev.index or 0)
-        return pynvml.nvmlDeviceGetHandleByIndex(idx)
+        self.nvml = None
 
     def _run(self):
-        import pynvml
         while not self.stop.is_set():
             try:
-                self.samples.append(pynvml.nvmlDeviceGetClockInfo(self.handle, pynvml.NVML_CLOCK_SM))
-                r = pynvml.nvmlDeviceGetCurrentClocksEventReasons(self.handle)
+                self.samples.append(self.nvml.clock(self.h))
+                r = self.nvml.reasons(self.h)
                 for n, bit in self.REASONS.items():
                     if r & bit:
                         self.reasons.add(n)
@@ -103,19 +132,19 @@ class ClockSampler:
 
     def __enter__(self):
         try:
-            import pynvml
-            self.handle = self._handle()
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.handle, pynvml.NVML_CLOCK_SM)
+            self.nvml = _Nvml()
+            self.h = self.nvml.handle(self.dev)
+            self.max_mhz = self.nvml.max_clock(self.h)
             self.thread = threading.Thread(target=self._run, daemon=True)
             self.thread.start()
-        except Exception as exc:  # clocks are reported as unavailable
+        except Exception as exc:  # clocks are then reported as unavailable
             self.error = repr(exc)
-            self.handle = None
+            self.nvml = None
         return self
 
     def __exit__(self, *a):
         self.stop.set()
-        if self.handle is not None:
+        if self.nvml is not None:
             self.thread.join(timeout=2)
 
     def summary(self):
@@ -135,6 +164,24 @@ def layer_work(w, counts_kept, n_dropped):
     router = 2.0 * N * d * E
     return {"rows": rows, "gemm1_flop": g1, "gemm2_flop": g2, "router_flop": router,
             "total_flop": g1 + g2 + router}
+
+
+def launches_per_step(w):
+    """Kernels of this library launched by one moe_forward with statistics."""
+    bf16 = w.dtype == synth.DT_BF16
+    # router logits, partial reduce (when K is split), finish, statistics
+    route = 3 + (1 if _route_split_ks(w, bf16) > 1 else 0)
+    dispatch = 3 + (1 if w.cap_mode == synth.CAP_REROUTE else 0)
+    return route + dispatch + 2 + 1
+
+
+def _route_split_ks(w, bf16):
+    tile = 128 if bf16 else 32
+    tiles = max(1, -(-w.n_tokens // tile))
+    kblocks = -(-w.d_model // 64)
+    ks = min(max(1, -(-296 // tiles)), kblocks)
+    k_slice = -(-kblocks // ks) * 64
+    return -(-w.d_model // k_slice)
 
 
 def to_dev(a, device):
@@ -312,9 +359,33 @@ def bench_ours(args, w):
         e2e_total = float(t[0])
 
     pk = peaks()
+    counts = st_t["counts"].cpu().numpy()
+    es = 2 if w.dtype == synth.DT_BF16 else 4
+    touched = int((counts > 0).sum()) + w.n_shared
+    nmat1 = 2 if w.act == synth.ACT_SWIGLU else 1
+    rows = work["rows"]
+    # algorithmic bytes of the first expert GEMM: weights of touched experts, its
+    # input rows, its output rows
+    g1_wbytes = touched * nmat1 * w.d_ff * w.d_model * es
+    g2_wbytes = touched * w.d_ff * w.d_model * es
+    g1_bytes = g1_wbytes + rows * w.d_model * es + rows * w.d_ff * es
     g1_ms = statistics.mean(stage["gemm1"])
     g1_tflops = work["gemm1_flop"] / (g1_ms * 1e-3) / 1e12
+    g1_gbs = g1_bytes / (g1_ms * 1e-3) / 1e9
     peak_t = pk["bf16_tflops_sustained"]
+    frac_t = g1_tflops / peak_t
+    frac_b = g1_gbs / pk["hbm_gbs"]
+    if frac_t >= frac_b:
+        roof = {"bound": "tensor", "achieved": g1_tflops, "peak": peak_t, "unit": "TFLOP/s",
+                "frac": frac_t, "peak_source": f"{pk['source']} bf16 sustained",
+                "frac_of_burst_peak": g1_tflops / pk["bf16_tflops"],
+                "algorithmic_per_launch": work["gemm1_flop"]}
+    else:
+        roof = {"bound": "hbm", "achieved": g1_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": frac_b, "peak_source": f"{pk['source']} copy bandwidth",
+                "algorithmic_per_launch": g1_bytes}
+    roof.update({"kernel": "ffn_tc_kernel<0> (gate/up GEMM + SwiGLU)", "traffic": None})
+    step_s = total_ms / args.steps * 1e-3
     tokens_total = w.n_tokens * args.steps * world
     value = tokens_total / (total_ms * 1e-3)
     line = {
@@ -323,19 +394,17 @@ def bench_ours(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == synth.DT_BF16 else "f32", "data": "synthetic",
         "config": workload_config(w, world),
-        "roofline": {"bound": "tensor", "kernel": "ffn_tc_kernel<0> (gate/up GEMM + SwiGLU)",
-                     "achieved": g1_tflops, "peak": peak_t, "unit": "TFLOP/s",
-                     "frac": g1_tflops / peak_t, "traffic": None,
-                     "peak_source": f"{pk['source']} bf16 sustained",
-                     "algorithmic_flop_per_launch": work["gemm1_flop"]},
+        "roofline": roof,
         "e2e": {"value": w.n_tokens * args.steps * world / (e2e_total * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x.numel() * x.element_size()),
                 "d2h_bytes_per_step": int(y.numel() * y.element_size())},
-        "gpu_launches": 8 * args.steps,
+        "gpu_launches": launches_per_step(w) * args.steps,
         "clocks": clk.summary(),
         "stages_ms": {k: statistics.mean(v) for k, v in stage.items()},
-        "layer_tflops": work["total_flop"] / (total_ms / args.steps * 1e-3) / 1e12,
-        "kept_assignments": kept, "dropped": nd,
+        "layer_tflops": work["total_flop"] / step_s / 1e12,
+        "layer_weight_gbs": (g1_wbytes + g2_wbytes) / step_s / 1e9,
+        "layer_weight_frac_hbm": (g1_wbytes + g2_wbytes) / step_s / 1e9 / pk["hbm_gbs"],
+        "experts_touched": touched, "kept_assignments": kept, "dropped": nd,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = run_cpu_oracle(w, inp, budget_s=args.ref_budget or 15.0,

@@ -21,7 +21,7 @@ constexpr int kTM = kRouteTM;   // tokens per CUDA-core logits CTA
 constexpr int kKC = 64;         // K chunk staged through shared memory
 constexpr int kXS = kKC + 4;    // padded smem row (floats), 16-byte aligned rows
 constexpr int kThreads = 256;
-constexpr int kFinishTokens = 64;   // tokens per finish CTA (8 warps x 8)
+constexpr int kWarps = kThreads / 32;
 
 __device__ __forceinline__ void load8f(const float* src, float (&v)[8]) {
   const float4 a = reinterpret_cast<const float4*>(src)[0];
@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kThreads) route_logits_simt(RouteParams p, Rou
 template <int EJ>
 __global__ void __launch_bounds__(kThreads) route_finish_kernel(RouteParams p, RouteSplit sp) {
   constexpr int EP = EJ * 32;
-  __shared__ float psum_w[kThreads / 32][EP];
+  __shared__ float psum_w[kWarps][EP];
   __shared__ int picks_s[EP];
   const int E = p.E, N = p.N, k = p.k;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -131,22 +131,16 @@ __global__ void __launch_bounds__(kThreads) route_finish_kernel(RouteParams p, R
   float psum[EJ];
 #pragma unroll
   for (int c = 0; c < EJ; ++c) psum[c] = 0.f;
-  const int tpw = kFinishTokens / (kThreads / 32);
+  const int tpw = route_finish_tpw(N);
   for (int i = 0; i < tpw; ++i) {
-    const int t = blockIdx.x * kFinishTokens + warp * tpw + i;
+    const int t = (blockIdx.x * kWarps + warp) * tpw + i;
     if (t >= N) break;
     float v[EJ];
     float m = -INFINITY;
 #pragma unroll
     for (int c = 0; c < EJ; ++c) {
       const int e = lane + 32 * c;
-      if (e < E) {
-        double z = 0.0;
-        for (int s = 0; s < sp.ks; ++s) z += (double)p.part[((size_t)s * N + t) * E + e];
-        v[c] = (float)z + (p.bias ? p.bias[e] : 0.f);
-      } else {
-        v[c] = -INFINITY;
-      }
+      v[c] = (e < E) ? p.part[(size_t)t * E + e] + (p.bias ? p.bias[e] : 0.f) : -INFINITY;
       m = fmaxf(m, v[c]);
     }
     m = warp_max(m);
@@ -199,10 +193,28 @@ __global__ void __launch_bounds__(kThreads) route_finish_kernel(RouteParams p, R
   // per-CTA partial statistics, warps summed in order (deterministic)
   for (int e = tid; e < E; e += kThreads) {
     float acc = 0.f;
-    for (int w = 0; w < kThreads / 32; ++w) acc += psum_w[w][e];
+    for (int w = 0; w < kWarps; ++w) acc += psum_w[w][e];
     p.psum_part[(size_t)blockIdx.x * E + e] = acc;
     p.picks_part[(size_t)blockIdx.x * E + e] = picks_s[e];
   }
+}
+
+// Logits from the K-slice partials: part[0][t][e] = sum_s part[s][t][e], summed
+// in double in slice order (8 independent loads in flight per thread).
+__global__ void __launch_bounds__(kThreads) route_reduce_kernel(float* part, int ks, size_t n) {
+  const size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x;
+  if (i >= n) return;
+  double z = 0.0;
+  int s = 0;
+  for (; s + 8 <= ks; s += 8) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = part[(size_t)(s + u) * n + i];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) z += (double)v[u];
+  }
+  for (; s < ks; ++s) z += (double)part[(size_t)s * n + i];
+  part[i] = (float)z;
 }
 
 // expert_freq, mean_prob and L_bal from the per-CTA partials: 4 threads per
@@ -270,7 +282,16 @@ cudaError_t launch_finish_t(const RouteParams& p, const RouteSplit& sp, cudaStre
 
 }  // namespace
 
-int route_finish_blocks(int N) { return (N + kFinishTokens - 1) / kFinishTokens; }
+// Tokens per finish warp: one for small batches (latency), up to 8 for large ones.
+__host__ __device__ int route_finish_tpw(int N) {
+  const int t = N / (148 * kWarps * 2);
+  return t < 1 ? 1 : (t > 8 ? 8 : t);
+}
+
+int route_finish_blocks(int N) {
+  const int per_cta = kWarps * route_finish_tpw(N);
+  return (N + per_cta - 1) / per_cta;
+}
 
 RouteSplit route_split(int N, int d, bool bf16) {
   const int tile = bf16 ? 128 : kTM;
@@ -294,6 +315,11 @@ cudaError_t launch_route(const RouteParams& p, bool bf16, cudaStream_t s) {
     err = [&]() -> cudaError_t { MOE_EJ_SWITCH(p.E, launch_simt_t, p, sp, s) }();
   }
   if (err != cudaSuccess) return err;
+  if (sp.ks > 1) {
+    const size_t n = (size_t)p.N * p.E;
+    route_reduce_kernel<<<(unsigned)((n + kThreads - 1) / kThreads), kThreads, 0, s>>>(p.part, sp.ks, n);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
   MOE_EJ_SWITCH(p.E, launch_finish_t, p, sp, s)
 }
 

@@ -6,12 +6,13 @@
 // One CTA per (128-token tile, K slice): TMA streams 128x64 tiles of x and
 // E_pad x 64 tiles of W_r (E padded to a multiple of 16, rows past E read as
 // zeros) through a 4-stage ring; one thread issues tcgen05.mma (M=128,
-// N=E_pad, K=16) into a TMEM accumulator; four epilogue warps read it back and
-// store fp32 partials.  Splitting K keeps >= 2 CTAs per SM busy even for
-// decode-sized batches, and keeps each fp32 accumulation short: the finish
-// kernel sums the slices in double, in slice order, so the logits stay within
-// ~1e-7 of the exact value and the top-k matches an exact evaluation except
-// on genuine near-ties.
+// N=E_pad, K=16); successive 64-deep K blocks rotate over up to 8 TMEM
+// accumulators so each fp32 accumulation stays a few MMAs long; four epilogue
+// warps add the accumulators in double and store fp32 partials.  Splitting K
+// keeps >= 2 CTAs per SM busy even for decode-sized batches; the reduce kernel
+// sums the slices in double, in slice order, so the logits stay within ~1e-7
+// of the exact value and the top-k matches an exact evaluation except on
+// genuine near-ties.
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -38,7 +39,7 @@ struct Ctrl {
 constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * (A_BYTES + MAX_B_BYTES) + sizeof(Ctrl);
 
 struct Params {
-  int N, E, d, e_pad, k_slice, tmem_cols;
+  int N, E, d, e_pad, k_slice, tmem_cols, acc_cols, nacc;
   float* part;
   int* status;
 };
@@ -50,7 +51,7 @@ route_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int b_bytes = p.e_pad * BK * 2;
-  const int stage_bytes = A_BYTES + b_bytes;           // multiple of 1024 (e_pad % 16 == 0... x128B)
+  const int stage_bytes = A_BYTES + b_bytes;           // a multiple of 1024 (e_pad % 16 == 0)
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + (size_t)STAGES * (A_BYTES + MAX_B_BYTES));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * BM;
@@ -97,9 +98,11 @@ route_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         const uint32_t a_addr = smem_u32(smem + (size_t)st * stage_bytes);
         const uint64_t adesc = sdesc_kmajor_sw128(a_addr);
         const uint64_t bdesc = sdesc_kmajor_sw128(a_addr + A_BYTES);
+        // K blocks rotate over nacc accumulators: each fp32 accumulation stays short
+        const uint32_t d = tmem + (uint32_t)((kb % p.nacc) * p.acc_cols);
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k)
-          umma_bf16(tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+          umma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb >= p.nacc) || k != 0);
         umma_commit(&ctrl->empty[st]);
       }
       if (ok) umma_commit(&ctrl->acc_full);
@@ -111,14 +114,22 @@ route_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
       tc_fence_after();
       const int t = t0 + q * 32 + lane;
       float* dst = p.part + ((size_t)ks * p.N + t) * p.E;
-      for (int c = 0; c < (p.e_pad + 31) / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c * 32, r);
-        tmem_wait_ld();
+      const int used = KB < p.nacc ? KB : p.nacc;
+      for (int c = 0; c < p.acc_cols / 32; ++c) {
+        double acc[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = 0.0;
+        for (int a = 0; a < used; ++a) {
+          uint32_t r[32];
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * p.acc_cols + c * 32), r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] += (double)__uint_as_float(r[i]);
+        }
         if (t < p.N) {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (c * 32 + i < p.E) dst[c * 32 + i] = __uint_as_float(r[i]);
+            if (c * 32 + i < p.E) dst[c * 32 + i] = (float)acc[i];
         }
       }
     }
@@ -164,9 +175,11 @@ cudaError_t launch_route_logits_tc(const RouteSplit& s, const void* x, const voi
   if (!encode(&mx, x, (uint64_t)N, (uint64_t)d, BM) ||
       !encode(&mw, w_router, (uint64_t)E, (uint64_t)d, (uint32_t)e_pad))
     return cudaErrorInvalidValue;
+  const int acc_cols = (e_pad + 31) / 32 * 32;
+  const int nacc = 512 / acc_cols < 8 ? 512 / acc_cols : 8;
   int cols = 32;
-  while (cols < e_pad) cols <<= 1;
-  Params p{N, E, d, e_pad, s.k_slice, cols, part, status};
+  while (cols < nacc * acc_cols) cols <<= 1;
+  Params p{N, E, d, e_pad, s.k_slice, cols, acc_cols, nacc, part, status};
   cudaError_t err = cudaFuncSetAttribute(route_logits_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
   if (err != cudaSuccess) return err;
