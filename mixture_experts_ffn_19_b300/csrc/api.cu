@@ -22,7 +22,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Layout {
   size_t status, topk_idx, topk_w, probs, final_idx, slot, pos, offsets, perm;
-  size_t part, psum_part, picks_part, chunk_cnt, local_rank, pend, rr_state, rr_scratch;
+  size_t part, psum_part, picks_part, chunk_cnt, local_rank, rr_state, rr_scratch;
   size_t x_perm, h, y_perm, total;
 };
 
@@ -56,7 +56,6 @@ Layout layout_of(const moe_config* c) {
   L.picks_part = take(rblocks * E * 4);
   L.chunk_cnt = take(chunks * E * 4);
   L.local_rank = take(N * k * 4);
-  L.pend = take(N * 4);
   L.rr_state = take(sizeof(RerouteState));
   L.rr_scratch = take(reroute_scratch_ints(c->n_tokens, c->top_k, c->n_experts) * 4);
   L.x_perm = take((size_t)max_rows_of(c) * c->d_model * es);
@@ -123,7 +122,6 @@ int dispatch_impl(const moe_config* c, const int32_t* topk_idx, const float* pro
   dp.local_rank = at<int32_t>(ws, L.local_rank);
   dp.final_idx = final_idx; dp.slot = at<int32_t>(ws, L.slot); dp.pos = pos;
   dp.offsets = offsets; dp.perm = perm; dp.x_perm = x_perm;
-  dp.pend = at<int32_t>(ws, L.pend);
   dp.rr = at<RerouteState>(ws, L.rr_state);
   dp.rr_prop = at<int32_t>(ws, L.rr_scratch);
   dp.rr_rank = dp.rr_prop + (size_t)c->n_tokens * c->top_k;

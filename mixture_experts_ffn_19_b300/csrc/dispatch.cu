@@ -12,17 +12,18 @@
 //   plan    one CTA: per-expert exclusive scan over the token chunks, so an
 //           assignment's rank within its expert is chunk base + local rank
 //           (its position in token order); capacity; segment offsets, counts
-//           and drop totals.  With reroute it instead marks the overflow
-//           pending and lists the tokens that have pending slots.
-//   reroute (reroute only) one cooperative launch of co-resident CTAs running
-//           the rounds, phases separated by a bounded grid barrier:
+//           and drop totals (reroute: initial fill levels only).
+//   reroute (reroute only) one cooperative launch of co-resident CTAs: the
+//           primary keep/pending decision per assignment, then the rounds,
+//           phases separated by a bounded grid barrier:
 //             A  every pending slot proposes the most probable expert (ties to
 //                the lower index) that was not full when the round started and
 //                that its token neither holds nor proposed earlier in the
 //                round (slots in slot order); bitmap ranks per chunk of tokens
 //             B  per-expert scan over the chunks; next fill levels
 //             C  an expert accepts proposals in token order while it has room
-//           then the segment layout, as plan does for the other modes.
+//           a round with no proposal ends it; then the segment layout, as plan
+//           does for the other modes.
 //   scatter one CTA per token: final expert, row, perm entry, and the 16-byte
 //           vector copy of x[t] into every row the token owns.
 #include "common.cuh"
@@ -150,36 +151,7 @@ __global__ void __launch_bounds__(kPlanThreads) dispatch_plan_kernel(DispatchPar
     return;
   }
 
-  // reroute: primary pass keeps rank < C and marks the rest pending
-  for (int a = tid; a < N * k; a += kPlanThreads) {
-    const int t = a / k;
-    const int e = p.topk_idx[a];
-    if (!valid_expert(e, E)) { p.final_idx[a] = -1; p.slot[a] = -1; continue; }
-    const int rank = p.chunk_cnt[(size_t)(t / kRankTC) * E + e] + p.local_rank[a];
-    if (rank < C) { p.final_idx[a] = e; p.slot[a] = rank; }
-    else { p.final_idx[a] = kPendingMark; p.slot[a] = -1; }
-  }
-  __syncthreads();
-  // tokens with a pending slot, in ascending order (block-wide compaction)
-  int base = 0;
-  for (int c0 = 0; c0 < N; c0 += kPlanThreads) {
-    const int t = c0 + tid;
-    bool f = false;
-    if (t < N)
-      for (int j = 0; j < k; ++j) f |= p.final_idx[(size_t)t * k + j] == kPendingMark;
-    const uint32_t bal = __ballot_sync(0xffffffffu, f);
-    if (lane == 0) warp_tot[warp] = __popc(bal);
-    __syncthreads();
-    if (tid == 0) {
-      int run = 0;
-      for (int w = 0; w < kPlanThreads / 32; ++w) { const int c = warp_tot[w]; warp_tot[w] = run; run += c; }
-      s_total = run;
-    }
-    __syncthreads();
-    if (f) p.pend[base + warp_tot[warp] + __popc(bal & lanemask_lt())] = t;
-    base += s_total;
-    __syncthreads();
-  }
+  // reroute: the cooperative kernel takes the assignments from here
   int kept = 0;
   for (int e = tid; e < E; e += kPlanThreads) { p.rr->fill[0][e] = fill[e]; kept += fill[e]; }
   kept = __reduce_add_sync(0xffffffffu, kept);
@@ -189,11 +161,10 @@ __global__ void __launch_bounds__(kPlanThreads) dispatch_plan_kernel(DispatchPar
     int s = 0;
     for (int w = 0; w < kPlanThreads / 32; ++w) s += warp_tot[w];
     p.rr->primary_kept = s;
-    p.rr->n_pending = base;
     p.rr->bar_count = 0;
     p.rr->bar_gen = 0;
   }
-  for (int r = tid; r < kMaxRounds; r += kPlanThreads) { p.rr->any_prop[r] = 0; p.rr->left[r] = 0; }
+  for (int r = tid; r < kMaxRounds; r += kPlanThreads) p.rr->any_prop[r] = 0;
 }
 
 // Grid-wide barrier for a cooperative launch (all CTAs co-resident).  Bounded:
@@ -223,62 +194,92 @@ __device__ void grid_barrier(RerouteState* rr, int* status) {
 }
 
 __global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchParams p) {
-  const int E = p.E, k = p.k, C = p.C;
+  const int E = p.E, k = p.k, C = p.C, N = p.N;
   RerouteState* rr = p.rr;
+  constexpr int TE = 64;                         // experts per staged probability tile
   __shared__ uint32_t bits[kMaxExperts * kRrWords];
+  __shared__ float prob_s[kRrThreads][TE + 1];
   __shared__ unsigned char full_s[kMaxExperts];
   __shared__ int fill_s[kMaxExperts];
   const int tid = threadIdx.x;
-  const int P = __ldcg(&rr->n_pending);
-  const int nch = (P + kRrThreads - 1) / kRrThreads;
-  int round = 0;
+  const int nch = (N + kRrThreads - 1) / kRrThreads;
+
+  // primary decisions: an assignment keeps its expert if its rank in token
+  // order (chunk base + rank inside the chunk) is below C, else it is pending
+  for (int c = blockIdx.x; c < nch; c += gridDim.x) {
+    const int t = c * kRrThreads + tid;
+    if (t >= N) continue;
+    for (int j = 0; j < k; ++j) {
+      const size_t a = (size_t)t * k + j;
+      const int e = p.topk_idx[a];
+      if (!valid_expert(e, E)) { p.final_idx[a] = -1; p.slot[a] = -1; continue; }
+      const int rank = p.chunk_cnt[(size_t)(t / kRankTC) * E + e] + p.local_rank[a];
+      if (rank < C) { p.final_idx[a] = e; p.slot[a] = rank; }
+      else { p.final_idx[a] = kPendingMark; p.slot[a] = -1; }
+    }
+  }
+
   int cur = 0;                                   // fill[cur] = levels at the start of the round
-  while (P > 0) {
+  for (int round = 0;; ++round) {
     if (round >= kMaxRounds || round > E + 1) { set_status(p.status, kDevBadState); break; }
-    // ---- phase A: proposals and per-chunk bitmap ranks
+    // ---- phase A: proposals, per-chunk bitmap ranks and counts
     for (int e = tid; e < E; e += kRrThreads) full_s[e] = __ldcg(&rr->fill[cur][e]) >= C;
     __syncthreads();
     for (int c = blockIdx.x; c < nch; c += gridDim.x) {
       for (int i = tid; i < E * kRrWords; i += kRrThreads) bits[i] = 0;
-      __syncthreads();
-      const int idx = c * kRrThreads + tid;
-      const int t = idx < P ? p.pend[idx] : -1;
-      int prop[kMaxTopk];
+      const int t = c * kRrThreads + tid;
+      int held[kMaxTopk], prop[kMaxTopk];
+      bool mine = false;
+      for (int j = 0; j < k; ++j) {
+        held[j] = t < N ? p.final_idx[(size_t)t * k + j] : -1;
+        prop[j] = -1;
+        mine |= held[j] == kPendingMark;
+      }
       bool any = false;
-      if (t >= 0) {
-        int held[kMaxTopk];
-        for (int j = 0; j < k; ++j) held[j] = p.final_idx[(size_t)t * k + j];
-        const float* pr = p.probs + (size_t)t * E;
+      bool tile_valid = false;                   // E <= TE: one staged tile serves every slot
+      if (__syncthreads_or(mine)) {
         for (int j = 0; j < k; ++j) {
-          prop[j] = -1;
-          if (held[j] != kPendingMark) continue;
+          const bool need = held[j] == kPendingMark;
+          if (!__syncthreads_or(need)) continue;
           float bp = -1.f;
           int be = -1;
-          for (int e0 = 0; e0 < E; e0 += 8) {
-            float pv[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) pv[u] = (e0 + u < E) ? pr[e0 + u] : -1.f;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int e = e0 + u;
-              if (e >= E || full_s[e]) continue;
-              bool skip = false;
-              for (int jj = 0; jj < k; ++jj) skip |= (held[jj] == e) | (jj < j && prop[jj] == e);
-              if (skip) continue;
-              if (be < 0 || better(pv[u], e, bp, be)) { bp = pv[u]; be = e; }
+          for (int e0 = 0; e0 < E; e0 += TE) {
+            if (E > TE || !tile_valid) {
+              tile_valid = true;
+              // stage probabilities [tokens of the chunk][e0, e0+TE) (coalesced)
+              __syncthreads();
+              for (int i = tid; i < kRrThreads * TE; i += kRrThreads) {
+                const int r = i / TE, col = i % TE;
+                const int tt = c * kRrThreads + r;
+                prob_s[r][col] = (tt < N && e0 + col < E) ? p.probs[(size_t)tt * E + e0 + col] : -1.f;
+              }
+              __syncthreads();
+            }
+            if (need) {
+              for (int col = 0; col < TE && e0 + col < E; ++col) {
+                const int e = e0 + col;
+                if (full_s[e]) continue;
+                bool skip = false;
+                for (int jj = 0; jj < k; ++jj) skip |= (held[jj] == e) | (jj < j && prop[jj] == e);
+                if (skip) continue;
+                const float pe = prob_s[tid][col];
+                if (be < 0 || better(pe, e, bp, be)) { bp = pe; be = e; }
+              }
             }
           }
-          prop[j] = be;
-          if (be < 0) {
-            p.final_idx[(size_t)t * k + j] = -1;          // nothing left: dropped
-          } else {
-            atomicOr(&bits[be * kRrWords + (tid >> 5)], 1u << (tid & 31));
-            any = true;
+          if (need) {
+            prop[j] = be;
+            if (be < 0) {
+              p.final_idx[(size_t)t * k + j] = -1;        // nothing left: dropped
+            } else {
+              atomicOr(&bits[be * kRrWords + (tid >> 5)], 1u << (tid & 31));
+              any = true;
+            }
           }
         }
       }
-      if (__syncthreads_or(any) && tid == 0) atomicExch(&rr->any_prop[round], 1);
-      if (t >= 0) {
+      __syncthreads();
+      if (mine) {
         for (int j = 0; j < k; ++j) {
           const int e = prop[j];
           int r = -1;
@@ -287,8 +288,8 @@ __global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchPa
             for (int w = 0; w < (tid >> 5); ++w) r += __popc(bits[e * kRrWords + w]);
             r += __popc(bits[e * kRrWords + (tid >> 5)] & lanemask_lt());
           }
-          p.rr_prop[(size_t)idx * k + j] = e;
-          p.rr_rank[(size_t)idx * k + j] = r;
+          p.rr_prop[(size_t)t * k + j] = e;
+          p.rr_rank[(size_t)t * k + j] = r;
         }
       }
       for (int e = tid; e < E; e += kRrThreads) {
@@ -296,9 +297,10 @@ __global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchPa
         for (int w = 0; w < kRrWords; ++w) n += __popc(bits[e * kRrWords + w]);
         p.rr_chunk[(size_t)c * E + e] = n;
       }
-      __syncthreads();
+      if (__syncthreads_or(any) && tid == 0) atomicExch(&rr->any_prop[round], 1);
     }
     grid_barrier(rr, p.status);
+    if (!__ldcg(&rr->any_prop[round])) break;    // nothing proposed: every slot is placed or dropped
     // ---- phase B: per-expert exclusive scan over chunks (a warp per expert),
     //      next fill levels
     {
@@ -313,39 +315,32 @@ __global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchPa
     // ---- phase C: acceptance in token order while the expert has room
     for (int e = tid; e < E; e += kRrThreads) fill_s[e] = __ldcg(&rr->fill[cur][e]);
     __syncthreads();
-    int left = 0;
     for (int c = blockIdx.x; c < nch; c += gridDim.x) {
-      const int idx = c * kRrThreads + tid;
-      if (idx >= P) continue;
-      const int t = p.pend[idx];
+      const int t = c * kRrThreads + tid;
+      if (t >= N) continue;
       for (int j = 0; j < k; ++j) {
-        const int e = p.rr_prop[(size_t)idx * k + j];
-        if (e < 0) continue;
-        const int s = fill_s[e] + __ldcg(&p.rr_chunk[(size_t)c * E + e]) + p.rr_rank[(size_t)idx * k + j];
-        if (s < C) { p.final_idx[(size_t)t * k + j] = e; p.slot[(size_t)t * k + j] = s; }
-        else ++left;
+        const size_t a = (size_t)t * k + j;
+        if (p.final_idx[a] != kPendingMark) continue;
+        const int e = p.rr_prop[a];
+        const int s = fill_s[e] + __ldcg(&p.rr_chunk[(size_t)c * E + e]) + p.rr_rank[a];
+        if (s < C) { p.final_idx[a] = e; p.slot[a] = s; }
       }
     }
-    if (__syncthreads_or(left > 0) && tid == 0) atomicExch(&rr->left[round], 1);
-    grid_barrier(rr, p.status);
+    __syncthreads();
     cur ^= 1;
-    const bool stop = !__ldcg(&rr->any_prop[round]) || !__ldcg(&rr->left[round]);
-    ++round;
-    if (stop) break;
   }
   // ---- layout from the final fill levels (CTA 0)
   if (blockIdx.x == 0) {
-    __syncthreads();
+    __shared__ int s_kept;
     for (int e = tid; e < E; e += kRrThreads) fill_s[e] = __ldcg(&rr->fill[cur][e]);
     __syncthreads();
-    __shared__ int s_kept;
     if (tid == 0) {
       int kept = 0;
       for (int e = 0; e < E; ++e) kept += fill_s[e];
       s_kept = kept;
     }
     __syncthreads();
-    write_layout(p, fill_s, p.N * k - s_kept, s_kept - __ldcg(&rr->primary_kept));
+    write_layout(p, fill_s, N * k - s_kept, s_kept - __ldcg(&rr->primary_kept));
   }
 }
 

@@ -53,8 +53,7 @@ constexpr int kMaxRounds = 260;   // reroute rounds never exceed E + 1 <= 257
 struct RerouteState {
   int fill[2][kMaxExperts];      // per-expert fill levels, double-buffered by round
   int any_prop[kMaxRounds];      // round r made at least one proposal
-  int left[kMaxRounds];          // round r left a proposal rejected
-  int primary_kept, n_pending;
+  int primary_kept;
   unsigned bar_count, bar_gen;   // grid barrier
 };
 size_t reroute_scratch_ints(int N, int k, int E);
@@ -73,10 +72,9 @@ struct DispatchParams {
   int32_t* offsets;          // [E+S+1]
   int32_t* perm;             // [max_rows]
   void* x_perm;              // [max_rows, d]
-  int32_t* pend;             // [N] scratch (pending token list)
   RerouteState* rr;          // reroute state (workspace)
-  int32_t* rr_prop;          // [N, k] proposals of the round
-  int32_t* rr_rank;          // [N, k] rank of each proposal inside its chunk
+  int32_t* rr_prop;          // [N, k] proposal of each pending slot in the round
+  int32_t* rr_rank;          // [N, k] rank of each proposal inside its 128-token chunk
   int32_t* rr_chunk;         // [ceil(N/128), E] per-chunk proposal counts, then bases
   int32_t* counts;           // [E] nullable
   int32_t* n_dropped;        // nullable

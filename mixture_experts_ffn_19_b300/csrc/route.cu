@@ -7,8 +7,8 @@
 // map, softmax, torch.topk, renormalise); «DeepSeek-V2 ...» summary §2.2
 // (expert_bias added to the logits before the softmax; load_balance_loss).
 //
-// The K-slice partials are summed in double in slice order, so the logits are
-// within ~1e-7 of the exact value and deterministic; top-k is k rounds of a
+// The K-slice partials are summed with compensation (fp32 Kahan) in slice order,
+// so the logits are within ~1e-7 of the exact value and deterministic; top-k is k rounds of a
 // warp-shuffle arg-max (higher probability first, ties to the lower index).
 #include "common.cuh"
 #include "kernels.h"
@@ -199,56 +199,56 @@ __global__ void __launch_bounds__(kThreads) route_finish_kernel(RouteParams p, R
   }
 }
 
-// Logits from the K-slice partials: part[0][t][e] = sum_s part[s][t][e], summed
-// in double in slice order (8 independent loads in flight per thread).
+// Logits from the K-slice partials: part[0][t][e] = sum_s part[s][t][e], a
+// compensated fp32 sum in slice order (8 independent loads in flight).
 __global__ void __launch_bounds__(kThreads) route_reduce_kernel(float* part, int ks, size_t n) {
   const size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x;
   if (i >= n) return;
-  double z = 0.0;
+  KahanF z;
   int s = 0;
   for (; s + 8 <= ks; s += 8) {
     float v[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) v[u] = part[(size_t)(s + u) * n + i];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) z += (double)v[u];
+    for (int u = 0; u < 8; ++u) z.add(v[u]);
   }
-  for (; s < ks; ++s) z += (double)part[(size_t)s * n + i];
-  part[i] = (float)z;
+  for (; s < ks; ++s) z.add(part[(size_t)s * n + i]);
+  part[i] = z.s;
 }
 
-// expert_freq, mean_prob and L_bal from the per-CTA partials: 4 threads per
-// expert each sum a fixed stride of rows in double, combined in a fixed order.
+// expert_freq, mean_prob and L_bal from the per-CTA partials: one warp per
+// expert, lanes take rows in a fixed stride (compensated fp32), then lane sums
+// are added in lane order; integer pick counts are exact.
 __global__ void __launch_bounds__(1024) route_stats_kernel(RouteStatsParams p) {
-  __shared__ double part_s[kMaxExperts][4];
-  __shared__ long long pick_s[kMaxExperts][4];
-  __shared__ double contrib[kMaxExperts];
-  const int e = threadIdx.x >> 2, q = threadIdx.x & 3;
-  if (e < p.E) {
-    double sp = 0.0;
+  __shared__ float contrib[kMaxExperts];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = warp; e < p.E; e += 32) {
+    KahanF sp;
     long long pk = 0;
-    for (int b = q; b < p.blocks; b += 4) {
-      sp += (double)p.psum_part[(size_t)b * p.E + e];
+    for (int b = lane; b < p.blocks; b += 32) {
+      sp.add(p.psum_part[(size_t)b * p.E + e]);
       pk += p.picks_part[(size_t)b * p.E + e];
     }
-    part_s[e][q] = sp;
-    pick_s[e][q] = pk;
-  }
-  __syncthreads();
-  if (e < p.E && q == 0) {
-    const double sp = ((part_s[e][0] + part_s[e][1]) + part_s[e][2]) + part_s[e][3];
-    const long long pk = pick_s[e][0] + pick_s[e][1] + pick_s[e][2] + pick_s[e][3];
-    const double mean = sp / (double)p.N;
-    const double freq = (double)pk / ((double)p.N * (double)p.k);
-    if (p.mean_prob) p.mean_prob[e] = (float)mean;
-    if (p.expert_freq) p.expert_freq[e] = (float)freq;
-    contrib[e] = freq * mean;
+    KahanF tot;
+    long long pks = 0;
+    for (int l = 0; l < 32; ++l) {
+      tot.add(__shfl_sync(0xffffffffu, sp.s, l));
+      pks += __shfl_sync(0xffffffffu, pk, l);
+    }
+    if (lane == 0) {
+      const float mean = tot.s / (float)p.N;
+      const float freq = (float)((double)pks / ((double)p.N * (double)p.k));
+      if (p.mean_prob) p.mean_prob[e] = mean;
+      if (p.expert_freq) p.expert_freq[e] = freq;
+      contrib[e] = freq * mean;
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0 && p.l_bal) {
-    double s = 0.0;
-    for (int i = 0; i < p.E; ++i) s += contrib[i];
-    p.l_bal[0] = (float)(p.E * s);
+    KahanF s;
+    for (int i = 0; i < p.E; ++i) s.add(contrib[i]);
+    p.l_bal[0] = (float)p.E * s.s;
   }
 }
 

@@ -8,9 +8,9 @@
 // zeros) through a 4-stage ring; one thread issues tcgen05.mma (M=128,
 // N=E_pad, K=16); successive 64-deep K blocks rotate over up to 8 TMEM
 // accumulators so each fp32 accumulation stays a few MMAs long; four epilogue
-// warps add the accumulators in double and store fp32 partials.  Splitting K
+// warps add the accumulators (compensated fp32) and store fp32 partials.  Splitting K
 // keeps >= 2 CTAs per SM busy even for decode-sized batches; the reduce kernel
-// sums the slices in double, in slice order, so the logits stay within ~1e-7
+// sums the slices (compensated fp32, in slice order), so the logits stay within ~1e-7
 // of the exact value and the top-k matches an exact evaluation except on
 // genuine near-ties.
 #include <mutex>
@@ -26,7 +26,6 @@ namespace {
 
 constexpr int BM = 128, BK = 64, STAGES = 4, NUM_THREADS = 192;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int MAX_B_BYTES = 256 * BK * 2;
 
 struct Ctrl {
   uint64_t full[STAGES];
@@ -36,7 +35,7 @@ struct Ctrl {
   int abort;
 };
 
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * (A_BYTES + MAX_B_BYTES) + sizeof(Ctrl);
+size_t smem_bytes(int e_pad) { return 1024 + (size_t)STAGES * (A_BYTES + e_pad * BK * 2) + sizeof(Ctrl); }
 
 struct Params {
   int N, E, d, e_pad, k_slice, tmem_cols, acc_cols, nacc;
@@ -52,7 +51,7 @@ route_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int b_bytes = p.e_pad * BK * 2;
   const int stage_bytes = A_BYTES + b_bytes;           // a multiple of 1024 (e_pad % 16 == 0)
-  Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + (size_t)STAGES * (A_BYTES + MAX_B_BYTES));
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + (size_t)STAGES * stage_bytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * BM;
   const int ks = blockIdx.y;
@@ -116,20 +115,18 @@ route_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
       float* dst = p.part + ((size_t)ks * p.N + t) * p.E;
       const int used = KB < p.nacc ? KB : p.nacc;
       for (int c = 0; c < p.acc_cols / 32; ++c) {
-        double acc[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = 0.0;
+        KahanF acc[32];
         for (int a = 0; a < used; ++a) {
           uint32_t r[32];
           tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * p.acc_cols + c * 32), r);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[i] += (double)__uint_as_float(r[i]);
+          for (int i = 0; i < 32; ++i) acc[i].add(__uint_as_float(r[i]));
         }
         if (t < p.N) {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (c * 32 + i < p.E) dst[c * 32 + i] = (float)acc[i];
+            if (c * 32 + i < p.E) dst[c * 32 + i] = acc[i].s;
         }
       }
     }
@@ -175,16 +172,18 @@ cudaError_t launch_route_logits_tc(const RouteSplit& s, const void* x, const voi
   if (!encode(&mx, x, (uint64_t)N, (uint64_t)d, BM) ||
       !encode(&mw, w_router, (uint64_t)E, (uint64_t)d, (uint32_t)e_pad))
     return cudaErrorInvalidValue;
+  // at most 256 TMEM columns per CTA, so two CTAs can share an SM
   const int acc_cols = (e_pad + 31) / 32 * 32;
-  const int nacc = 512 / acc_cols < 8 ? 512 / acc_cols : 8;
+  const int nacc = 256 / acc_cols < 1 ? 1 : (256 / acc_cols < 8 ? 256 / acc_cols : 8);
   int cols = 32;
   while (cols < nacc * acc_cols) cols <<= 1;
   Params p{N, E, d, e_pad, s.k_slice, cols, acc_cols, nacc, part, status};
+  const size_t smem = smem_bytes(e_pad);
   cudaError_t err = cudaFuncSetAttribute(route_logits_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+                                         (int)smem);
   if (err != cudaSuccess) return err;
   dim3 grid((N + BM - 1) / BM, s.ks);
-  route_logits_tc<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(mx, mw, p);
+  route_logits_tc<<<grid, NUM_THREADS, smem, stream>>>(mx, mw, p);
   return cudaGetLastError();
 }
 
