@@ -40,6 +40,22 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", 1)))
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0])
+
+
+def throughput(tokens_per_step: int, steps: int, world: int, total_ms: float) -> float:
+    """Whole-job tokens/s: every rank processes its own batch (weak scaling)."""
+    return tokens_per_step * steps * world / (total_ms * 1e-3)
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -324,11 +340,7 @@ def bench_ours(args, w):
     step_ms = [evs[s][0].elapsed_time(evs[s][5]) for s in range(args.steps)]
     stage = {n: [evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps)]
              for i, n in enumerate(["route", "dispatch", "gemm1", "gemm2", "combine"])}
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t[0])
+    total_ms = max_over_ranks(sum(step_ms), dev)
     st = moe.moe_device_status(ws)
     if st != moe.MOE_OK:
         raise RuntimeError(f"device status {moe.status_string(st)}")
@@ -352,11 +364,7 @@ def bench_ours(args, w):
         e1.synchronize()
         if s >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_total = sum(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t[0])
+    e2e_total = max_over_ranks(sum(e2e_ms), dev)
 
     pk = peaks()
     counts = st_t["counts"].cpu().numpy()
@@ -386,8 +394,7 @@ def bench_ours(args, w):
                 "algorithmic_per_launch": g1_bytes}
     roof.update({"kernel": "ffn_tc_kernel<0> (gate/up GEMM + SwiGLU)", "traffic": None})
     step_s = total_ms / args.steps * 1e-3
-    tokens_total = w.n_tokens * args.steps * world
-    value = tokens_total / (total_ms * 1e-3)
+    value = throughput(w.n_tokens, args.steps, world, total_ms)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
@@ -395,7 +402,7 @@ def bench_ours(args, w):
         "dtype": "bf16" if w.dtype == synth.DT_BF16 else "f32", "data": "synthetic",
         "config": workload_config(w, world),
         "roofline": roof,
-        "e2e": {"value": w.n_tokens * args.steps * world / (e2e_total * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": throughput(w.n_tokens, args.steps, world, e2e_total), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x.numel() * x.element_size()),
                 "d2h_bytes_per_step": int(y.numel() * y.element_size())},
         "gpu_launches": launches_per_step(w) * args.steps,
