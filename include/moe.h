@@ -214,6 +214,27 @@ int moe_forward(const moe_config* cfg, const void* x, const void* w_router,
                 const moe_stats* stats, void* workspace, size_t workspace_bytes,
                 void* stream, const moe_timing* timing);
 
+/* Dispatch without a workspace.  No page has a counterpart: it exists for
+ * callers that cannot allocate device memory when they run the layer (a
+ * serving process that reserved all its memory up front, or a loop that must
+ * not pay the device synchronisation cudaMalloc/cudaFree may cause).  Same
+ * arguments and results as moe_dispatch, with the scratch kept in a fixed
+ * 8 MiB device array inside the library, which every GPU that loads the
+ * library holds until exit; nothing is allocated.
+ *   device_status  [1] int32 out, nullable: cleared by the call, then set to a
+ *                  nonzero code by a device-side failure (1 = a wait timed
+ *                  out, 2 = a bad expert index or internal check).
+ * Returns MOE_ERR_WORKSPACE when the scratch for these sizes exceeds 8 MiB
+ * (about 60k tokens at E=256, k=8).  The first call on a device looks up the
+ * array's address (cudaGetSymbolAddress, once per device): make it before any
+ * stream capture.  All calls share the array and it keeps the previous call's
+ * contents (each call clears what must start at zero); calls whose kernels
+ * overlap on the GPU race and give wrong results. */
+int moe_dispatch_noalloc(const moe_config* cfg, const int32_t* topk_idx, const float* probs,
+                         const void* x, int32_t* final_idx, int32_t* pos, int32_t* offsets,
+                         int32_t* perm, void* x_perm, const moe_stats* stats,
+                         int32_t* device_status, void* stream);
+
 /* Synchronises `stream`, then copies the workspace's device status word to
  * *status_out (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE) and clears it. */
 int moe_device_status(void* workspace, void* stream, int32_t* status_out);
