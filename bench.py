@@ -185,8 +185,8 @@ def layer_work(w, counts_kept, n_dropped):
 def launches_per_step(w):
     """Kernels of this library launched by one moe_forward with statistics."""
     bf16 = w.dtype == synth.DT_BF16
-    # router logits, partial reduce (when K is split), finish, statistics
-    route = 3 + (1 if _route_split_ks(w, bf16) > 1 else 0)
+    # router logits, partial reduce (when K is split), finish (+ statistics)
+    route = 2 + (1 if _route_split_ks(w, bf16) > 1 else 0)
     dispatch = 3 + (1 if w.cap_mode == synth.CAP_REROUTE else 0)
     return route + dispatch + 2 + 1
 

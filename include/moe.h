@@ -26,8 +26,12 @@
  *   - A call returns MOE_OK after enqueueing, or a negative moe_status from the
  *     host-side checks done before any launch; then nothing was written.
  *     A failed launch returns MOE_ERR_CUDA.
- *   - Device-side failures (a bounded wait that ran out) are recorded in a
- *     status word inside the workspace; read it with moe_device_status().
+ *   - Device-side failures (a bounded wait that ran out, an expert index out
+ *     of range) are recorded in a status word inside the workspace; read it
+ *     with moe_device_status().  moe_route and moe_forward clear it (and the
+ *     statistics accumulators next to it) when they start; moe_dispatch and
+ *     moe_expert_ffn only add to it, so a fresh workspace used first by one of
+ *     those must be zero-filled once (or moe_device_status called once).
  *   - Layouts are row-major.  Weight matrices are nn.Linear style [out, in].
  *     Shared experts are experts E .. E+S-1 of the expert weight arrays.
  *   - dtype MOE_BF16: x, w_router, expert weights, x_perm, y_perm and y are

@@ -21,8 +21,9 @@ int64_t align_rows(int64_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Layout {
-  size_t status, topk_idx, topk_w, probs, final_idx, slot, pos, offsets, perm;
-  size_t part, psum_part, picks_part, chunk_cnt, local_rank, rr_state, rr_scratch;
+  size_t status, acc_p, acc_pick, ticket, zero_end;  // [status .. zero_end) is cleared per call
+  size_t topk_idx, topk_w, probs, final_idx, slot, pos, offsets, perm;
+  size_t part, chunk_cnt, local_rank, rr_state, rr_scratch;
   size_t x_perm, h, y_perm, total;
 };
 
@@ -37,12 +38,15 @@ Layout layout_of(const moe_config* c) {
   Layout L;
   const size_t N = (size_t)c->n_tokens, k = (size_t)c->top_k, E = (size_t)c->n_experts;
   const size_t es = c->dtype == MOE_BF16 ? 2 : 4;
-  const size_t rblocks = (size_t)route_finish_blocks(c->n_tokens);
   const RouteSplit rs = route_split(c->n_tokens, c->d_model, c->dtype == MOE_BF16);
   const size_t chunks = (N + kRankTC - 1) / kRankTC;
   size_t off = 0;
   auto take = [&](size_t bytes) { const size_t o = off; off = align_up(off + bytes, kWsAlign); return o; };
   L.status = take(sizeof(int32_t));
+  L.acc_p = take(E * 8);
+  L.acc_pick = take(E * 4);
+  L.ticket = take(4);
+  L.zero_end = off;
   L.topk_idx = take(N * k * 4);
   L.topk_w = take(N * k * 4);
   L.probs = take(N * E * 4);
@@ -52,8 +56,6 @@ Layout layout_of(const moe_config* c) {
   L.offsets = take((E + c->n_shared + 1) * 4);
   L.perm = take((size_t)max_rows_of(c) * 4);
   L.part = take((size_t)rs.ks * N * E * 4);
-  L.psum_part = take(rblocks * E * 4);
-  L.picks_part = take(rblocks * E * 4);
   L.chunk_cnt = take(chunks * E * 4);
   L.local_rank = take(N * k * 4);
   L.rr_state = take(sizeof(RerouteState));
@@ -96,17 +98,17 @@ int route_impl(const moe_config* c, const void* x, const void* w_router, const f
                int32_t* topk_idx, float* topk_w, float* probs, const moe_stats* stats, void* ws,
                cudaStream_t s) {
   const Layout L = layout_of(c);
-  RouteParams rp{x, w_router, c->has_router_bias ? bias : nullptr, c->n_tokens, c->d_model,
-                 c->n_experts, c->top_k, topk_idx, topk_w, probs, at<float>(ws, L.part),
-                 at<float>(ws, L.psum_part), at<int32_t>(ws, L.picks_part), at<int>(ws, L.status)};
-  if (launch_route(rp, c->dtype == MOE_BF16, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (stats && (stats->expert_freq || stats->mean_prob || stats->l_bal)) {
-    RouteStatsParams sp{rp.psum_part, rp.picks_part, route_finish_blocks(c->n_tokens),
-                        c->n_tokens, c->n_experts, c->top_k, stats->expert_freq,
-                        stats->mean_prob, stats->l_bal};
-    if (launch_route_stats(sp, s) != cudaSuccess) return MOE_ERR_CUDA;
-  }
-  return MOE_OK;
+  RouteParams rp{};
+  rp.x = x; rp.w_router = w_router; rp.bias = c->has_router_bias ? bias : nullptr;
+  rp.N = c->n_tokens; rp.d = c->d_model; rp.E = c->n_experts; rp.k = c->top_k;
+  rp.topk_idx = topk_idx; rp.topk_w = topk_w; rp.probs = probs;
+  rp.part = at<float>(ws, L.part);
+  rp.acc_p = at<unsigned long long>(ws, L.acc_p);
+  rp.acc_pick = at<int>(ws, L.acc_pick);
+  rp.ticket = at<unsigned>(ws, L.ticket);
+  if (stats) { rp.expert_freq = stats->expert_freq; rp.mean_prob = stats->mean_prob; rp.l_bal = stats->l_bal; }
+  rp.status = at<int>(ws, L.status);
+  return launch_route(rp, c->dtype == MOE_BF16, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 int dispatch_impl(const moe_config* c, const int32_t* topk_idx, const float* probs, const void* x,
@@ -243,7 +245,7 @@ int moe_route(const moe_config* c, const void* x, const void* w_router, const fl
   if (c->has_router_bias && !bias) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(at<int>(ws, layout_of(c).status), 0, sizeof(int), s) != cudaSuccess)
+  if (cudaMemsetAsync(ws, 0, layout_of(c).zero_end, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (c->n_tokens == 0) return MOE_OK;
   return route_impl(c, x, w_router, bias, topk_idx, topk_w, probs, stats, ws, s);
@@ -309,7 +311,7 @@ int moe_forward(const moe_config* c, const void* x, const void* w_router, const 
     return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Layout L = layout_of(c);
-  if (cudaMemsetAsync(at<int>(ws, L.status), 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, L.zero_end, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (c->n_tokens == 0) return MOE_OK;
   float* probs = c->cap_mode == MOE_CAP_REROUTE ? at<float>(ws, L.probs) : nullptr;
   record(timing, 0, s);

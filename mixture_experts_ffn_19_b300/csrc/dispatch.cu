@@ -246,12 +246,23 @@ __global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchPa
           for (int e0 = 0; e0 < E; e0 += TE) {
             if (E > TE || !tile_valid) {
               tile_valid = true;
-              // stage probabilities [tokens of the chunk][e0, e0+TE) (coalesced)
+              // stage probabilities [tokens of the chunk][e0, e0+TE): coalesced,
+              // 16 independent loads in flight per thread
               __syncthreads();
-              for (int i = tid; i < kRrThreads * TE; i += kRrThreads) {
-                const int r = i / TE, col = i % TE;
-                const int tt = c * kRrThreads + r;
-                prob_s[r][col] = (tt < N && e0 + col < E) ? p.probs[(size_t)tt * E + e0 + col] : -1.f;
+              for (int i0 = 0; i0 < kRrThreads * TE; i0 += kRrThreads * 16) {
+                float v[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                  const int i = i0 + u * kRrThreads + tid;
+                  const int r = i / TE, col = i % TE;
+                  const int tt = c * kRrThreads + r;
+                  v[u] = (tt < N && e0 + col < E) ? __ldcg(&p.probs[(size_t)tt * E + e0 + col]) : -1.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                  const int i = i0 + u * kRrThreads + tid;
+                  prob_s[i / TE][i % TE] = v[u];
+                }
               }
               __syncthreads();
             }

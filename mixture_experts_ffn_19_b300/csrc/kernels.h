@@ -22,8 +22,15 @@ struct RouteParams {
   float* topk_w;             // [N, k]
   float* probs;              // [N, E] or null
   float* part;               // [ks, N, E] partial logits (one per K slice)
-  float* psum_part;          // [route_finish_blocks(N), E]
-  int32_t* picks_part;       // [route_finish_blocks(N), E]
+  // load-balance statistics: exact fixed-point sums of p (2^-40 units) and pick
+  // counts, accumulated across CTAs (zeroed before the router runs); the last
+  // CTA to finish turns them into the outputs below (each nullable)
+  unsigned long long* acc_p; // [E]
+  int* acc_pick;             // [E]
+  unsigned* ticket;          // [1]
+  float* expert_freq;        // [E]
+  float* mean_prob;          // [E]
+  float* l_bal;              // [1]
   int* status;
 };
 
@@ -38,14 +45,6 @@ cudaError_t launch_route_logits_tc(const RouteSplit& s, const void* x, const voi
                                    int N, int E, int d, float* part, int* status,
                                    cudaStream_t stream);
 
-struct RouteStatsParams {
-  const float* psum_part;
-  const int32_t* picks_part;
-  int blocks, N, E, k;
-  float* expert_freq;        // nullable
-  float* mean_prob;          // nullable
-  float* l_bal;              // nullable
-};
 
 constexpr int kMaxRounds = 260;   // reroute rounds never exceed E + 1 <= 257
 
@@ -110,7 +109,6 @@ struct CombineParams {
 };
 
 cudaError_t launch_route(const RouteParams& p, bool bf16, cudaStream_t s);
-cudaError_t launch_route_stats(const RouteStatsParams& p, cudaStream_t s);
 cudaError_t launch_dispatch(const DispatchParams& p, bool bf16, cudaStream_t s);
 cudaError_t launch_ffn_simt(const FfnParams& p, cudaStream_t s, cudaEvent_t mid);
 cudaError_t launch_ffn_tc(const FfnParams& p, cudaStream_t s, cudaEvent_t mid);

@@ -1,7 +1,8 @@
 // Router: partial logits (fp32 layers: CUDA-core contraction here; bf16 layers:
-// tensor cores, route_tc.cu), then a warp-per-token finish: sum of the K-slice
-// partials, router bias, fp32 softmax, top-k with renormalised gates, and the
-// per-CTA partial sums of the load-balance statistics.
+// tensor cores, route_tc.cu), their reduction over K slices, then a
+// warp-per-token finish: router bias, fp32 softmax, top-k with renormalised
+// gates, and the load-balance statistics (exact fixed-point sums across CTAs,
+// finished by the last CTA).
 //
 // «为什么MoE有效？稀疏激活的数学直觉与工程实践» §2.2 (router = bias-free linear
 // map, softmax, torch.topk, renormalise); «DeepSeek-V2 ...» summary §2.2
@@ -122,15 +123,16 @@ __global__ void __launch_bounds__(kThreads) route_logits_simt(RouteParams p, Rou
 template <int EJ>
 __global__ void __launch_bounds__(kThreads) route_finish_kernel(RouteParams p, RouteSplit sp) {
   constexpr int EP = EJ * 32;
-  __shared__ float psum_w[kWarps][EP];
+  __shared__ unsigned long long psum_w[kWarps][EP];
   __shared__ int picks_s[EP];
+  __shared__ bool last_cta;
   const int E = p.E, N = p.N, k = p.k;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int e = tid; e < EP; e += kThreads) picks_s[e] = 0;
   __syncthreads();
-  float psum[EJ];
+  unsigned long long psum[EJ];                  // sum of p in units of 2^-40 (exact)
 #pragma unroll
-  for (int c = 0; c < EJ; ++c) psum[c] = 0.f;
+  for (int c = 0; c < EJ; ++c) psum[c] = 0ull;
   const int tpw = route_finish_tpw(N);
   for (int i = 0; i < tpw; ++i) {
     const int t = (blockIdx.x * kWarps + warp) * tpw + i;
@@ -156,7 +158,7 @@ __global__ void __launch_bounds__(kThreads) route_finish_kernel(RouteParams p, R
       const int e = lane + 32 * c;
       v[c] = v[c] / s;
       if (e < E) {
-        psum[c] += v[c];
+        psum[c] += __float2ull_rn(v[c] * 1099511627776.0f);
         if (p.probs) p.probs[(size_t)t * E + e] = v[c];
       }
     }
@@ -190,12 +192,33 @@ __global__ void __launch_bounds__(kThreads) route_finish_kernel(RouteParams p, R
 #pragma unroll
   for (int c = 0; c < EJ; ++c) psum_w[warp][lane + 32 * c] = psum[c];
   __syncthreads();
-  // per-CTA partial statistics, warps summed in order (deterministic)
+  // integer sums are exact, so the cross-CTA atomics are order-independent
   for (int e = tid; e < E; e += kThreads) {
-    float acc = 0.f;
+    unsigned long long acc = 0ull;
     for (int w = 0; w < kWarps; ++w) acc += psum_w[w][e];
-    p.psum_part[(size_t)blockIdx.x * E + e] = acc;
-    p.picks_part[(size_t)blockIdx.x * E + e] = picks_s[e];
+    atomicAdd(&p.acc_p[e], acc);
+    atomicAdd(&p.acc_pick[e], picks_s[e]);
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) last_cta = atomicAdd(p.ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last_cta) return;
+  // the last CTA: expert_freq, mean_prob and L_bal («DeepSeek-V2 ...» summary §2.2)
+  __threadfence();
+  __shared__ float contrib[kMaxExperts];
+  for (int e = tid; e < E; e += kThreads) {
+    const float mean = __ull2float_rn(__ldcg(&p.acc_p[e])) * (1.0f / 1099511627776.0f) / (float)N;
+    const float freq = (float)__ldcg(&p.acc_pick[e]) / ((float)N * (float)k);
+    if (p.mean_prob) p.mean_prob[e] = mean;
+    if (p.expert_freq) p.expert_freq[e] = freq;
+    contrib[e] = freq * mean;
+  }
+  __syncthreads();
+  if (tid == 0 && p.l_bal) {
+    KahanF s;
+    for (int e = 0; e < E; ++e) s.add(contrib[e]);
+    p.l_bal[0] = (float)E * s.s;
   }
 }
 
@@ -215,41 +238,6 @@ __global__ void __launch_bounds__(kThreads) route_reduce_kernel(float* part, int
   }
   for (; s < ks; ++s) z.add(part[(size_t)s * n + i]);
   part[i] = z.s;
-}
-
-// expert_freq, mean_prob and L_bal from the per-CTA partials: one warp per
-// expert, lanes take rows in a fixed stride (compensated fp32), then lane sums
-// are added in lane order; integer pick counts are exact.
-__global__ void __launch_bounds__(1024) route_stats_kernel(RouteStatsParams p) {
-  __shared__ float contrib[kMaxExperts];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int e = warp; e < p.E; e += 32) {
-    KahanF sp;
-    long long pk = 0;
-    for (int b = lane; b < p.blocks; b += 32) {
-      sp.add(p.psum_part[(size_t)b * p.E + e]);
-      pk += p.picks_part[(size_t)b * p.E + e];
-    }
-    KahanF tot;
-    long long pks = 0;
-    for (int l = 0; l < 32; ++l) {
-      tot.add(__shfl_sync(0xffffffffu, sp.s, l));
-      pks += __shfl_sync(0xffffffffu, pk, l);
-    }
-    if (lane == 0) {
-      const float mean = tot.s / (float)p.N;
-      const float freq = (float)((double)pks / ((double)p.N * (double)p.k));
-      if (p.mean_prob) p.mean_prob[e] = mean;
-      if (p.expert_freq) p.expert_freq[e] = freq;
-      contrib[e] = freq * mean;
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0 && p.l_bal) {
-    KahanF s;
-    for (int i = 0; i < p.E; ++i) s.add(contrib[i]);
-    p.l_bal[0] = (float)p.E * s.s;
-  }
 }
 
 template <int EJ>
@@ -323,9 +311,5 @@ cudaError_t launch_route(const RouteParams& p, bool bf16, cudaStream_t s) {
   MOE_EJ_SWITCH(p.E, launch_finish_t, p, sp, s)
 }
 
-cudaError_t launch_route_stats(const RouteStatsParams& p, cudaStream_t s) {
-  route_stats_kernel<<<1, 1024, 0, s>>>(p);
-  return cudaGetLastError();
-}
 
 }  // namespace moe
