@@ -182,6 +182,26 @@ def layer_work(w, counts_kept, n_dropped):
             "total_flop": g1 + g2 + router}
 
 
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from a committed ncu capture
+    (profiles/ncu_traffic.json), or None when there is none or the kernel's source
+    has changed since it was taken (sha256 of its source files)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            entry = json.load(f)[workload][kernel]
+        h = hashlib.sha256()
+        for src in entry["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != entry["source_sha256"]:
+            return None
+        return float(entry["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def launches_per_step(w):
     """Kernels of this library launched by one moe_forward with statistics."""
     bf16 = w.dtype == synth.DT_BF16
@@ -392,7 +412,9 @@ def bench_ours(args, w):
         roof = {"bound": "hbm", "achieved": g1_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": frac_b, "peak_source": f"{pk['source']} copy bandwidth",
                 "algorithmic_per_launch": g1_bytes}
-    roof.update({"kernel": "ffn_tc_kernel<0> (gate/up GEMM + SwiGLU)", "traffic": None})
+    roof.update({"kernel": "ffn_tc_kernel<0> (gate/up GEMM + SwiGLU)",
+                 "traffic": measured_traffic("ffn_tc_kernel<0>", w.name),
+                 "algorithmic_bytes_per_launch": g1_bytes})
     step_s = total_ms / args.steps * 1e-3
     value = throughput(w.n_tokens, args.steps, world, total_ms)
     line = {
