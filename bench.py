@@ -202,6 +202,30 @@ def measured_traffic(kernel: str, workload: str):
         return None
 
 
+TRAFFIC_SOURCES = {
+    "ffn_tc_kernel<0>": ["mixture_experts_ffn_19_b300/csrc/ffn_tc.cu",
+                         "mixture_experts_ffn_19_b300/csrc/common.cuh"],
+}
+
+
+def record_traffic(workload: str, kernel: str, nbytes: float, command: str) -> None:
+    """Store one ncu capture's DRAM bytes per launch in profiles/ncu_traffic.json with
+    the sha256 of the kernel's sources (read back by measured_traffic)."""
+    import hashlib
+    srcs = TRAFFIC_SOURCES[kernel]
+    h = hashlib.sha256()
+    for s in srcs:
+        with open(os.path.join(ROOT, s), "rb") as f:
+            h.update(f.read())
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    data = json.load(open(path)) if os.path.exists(path) else {}
+    data.setdefault(workload, {})[kernel] = {
+        "dram_bytes_per_launch": float(nbytes), "sources": srcs,
+        "source_sha256": h.hexdigest(), "command": command}
+    with open(path, "w") as f:
+        json.dump(data, f, indent=1, sort_keys=True)
+
+
 def launches_per_step(w):
     """Kernels of this library launched by one moe_forward with statistics."""
     bf16 = w.dtype == synth.DT_BF16
@@ -459,7 +483,13 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=None)
     ap.add_argument("--set", action="append", default=[], metavar="FIELD=VALUE",
                     help="override a workload field (e.g. n_experts=2) for a smaller case")
+    ap.add_argument("--record-traffic", nargs=4, metavar=("WORKLOAD", "KERNEL", "BYTES", "COMMAND"),
+                    help="store an ncu capture's DRAM bytes per launch for the roofline record")
     args = ap.parse_args(argv)
+    if args.record_traffic:
+        wl, kern, nb, cmd = args.record_traffic
+        record_traffic(wl, kern, float(nb), cmd)
+        return 0
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     w = synth.WORKLOADS[args.workload]
