@@ -226,24 +226,6 @@ def record_traffic(workload: str, kernel: str, nbytes: float, command: str) -> N
         json.dump(data, f, indent=1, sort_keys=True)
 
 
-def launches_per_step(w):
-    """Kernels of this library launched by one moe_forward with statistics."""
-    bf16 = w.dtype == synth.DT_BF16
-    # router logits, partial reduce (when K is split), finish (+ statistics)
-    route = 2 + (1 if _route_split_ks(w, bf16) > 1 else 0)
-    dispatch = 3 + (1 if w.cap_mode == synth.CAP_REROUTE else 0)
-    return route + dispatch + 2 + 1
-
-
-def _route_split_ks(w, bf16):
-    tile = 128 if bf16 else 32
-    tiles = max(1, -(-w.n_tokens // tile))
-    kblocks = -(-w.d_model // 64)
-    ks = min(max(1, -(-296 // tiles)), kblocks)
-    k_slice = -(-kblocks // ks) * 64
-    return -(-w.d_model // k_slice)
-
-
 def to_dev(a, device):
     import torch
     if a is None:
@@ -374,11 +356,13 @@ def bench_ours(args, w):
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
+    launches0 = moe.moe_kernel_launches()
     with ClockSampler(dev) as clk:
         for s in range(args.steps):
             flush.fill_(s & 0xFF)
             moe.moe_forward(*args_f, stats, ws, stream, timing=timings[s])
         torch.cuda.synchronize()
+    launches = moe.moe_kernel_launches() - launches0
     if world > 1:
         dist.barrier()
     step_ms = [evs[s][0].elapsed_time(evs[s][5]) for s in range(args.steps)]
@@ -451,7 +435,7 @@ def bench_ours(args, w):
         "e2e": {"value": throughput(w.n_tokens, args.steps, world, e2e_total), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x.numel() * x.element_size()),
                 "d2h_bytes_per_step": int(y.numel() * y.element_size())},
-        "gpu_launches": launches_per_step(w) * args.steps,
+        "gpu_launches": launches,
         "clocks": clk.summary(),
         "stages_ms": {k: statistics.mean(v) for k, v in stage.items()},
         "layer_tflops": work["total_flop"] / step_s / 1e12,

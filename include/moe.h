@@ -152,6 +152,10 @@ size_t moe_workspace_size(const moe_config* cfg);
 int moe_workspace_views(const moe_config* cfg, void* workspace, size_t workspace_bytes,
                         moe_views* out);
 
+/* Number of CUDA kernels this library has launched in this process so far
+ * (host-side count, every entry point included). */
+int64_t moe_kernel_launches(void);
+
 /* ---- device calls ---------------------------------------------------------- */
 
 /* Router: logits, fp32 softmax, top-k with renormalised gates, and the
@@ -188,8 +192,11 @@ int moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const float* pr
 /* Expert FFNs of every segment as one grouped computation.
  *   x       [N, d]   in (rows of the shared-expert segments)
  *   x_perm  [moe_max_rows, d] in (rows of the routed segments)
- *   offsets [E+S+1]  in (segment layout from moe_dispatch; every segment
- *           length a multiple of MOE_SEGMENT_ALIGN except as produced there)
+ *   offsets [E+S+1]  in (segment layout from moe_dispatch)
+ *   counts  [E]      in, nullable: kept rows per routed expert (stats->counts
+ *           of moe_dispatch).  With counts, batches with few tokens per expert
+ *           run a variant with the weights as the wide MMA operand; without,
+ *           every padded row of every segment is computed (same results)
  *   w_gate  [E+S, F, d]  SwiGLU gate weight | GELU W1
  *   w_up    [E+S, F, d]  SwiGLU up weight   | GELU: NULL
  *   w_down  [E+S, d, F]  down weight (W2)
@@ -198,9 +205,9 @@ int moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const float* pr
  * bf16 runs on the tensor cores (fp32 accumulation, the SwiGLU product is
  * rounded to bf16 between the two GEMMs); fp32 runs in fp32 on the CUDA cores. */
 int moe_expert_ffn(const moe_config* cfg, const void* x, const void* x_perm,
-                   const int32_t* offsets, const void* w_gate, const void* w_up,
-                   const void* w_down, const void* b1, const void* b2, void* y_perm,
-                   void* workspace, size_t workspace_bytes, void* stream);
+                   const int32_t* offsets, const int32_t* counts, const void* w_gate,
+                   const void* w_up, const void* w_down, const void* b1, const void* b2,
+                   void* y_perm, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Combine: y[t] = sum_s y_perm[offsets[E+s] + t] + sum_j topk_w[t,j] *
  * y_perm[pos[t,j]] over kept slots, summed in fp32 in that fixed order.

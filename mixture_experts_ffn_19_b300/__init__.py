@@ -75,13 +75,14 @@ _SIGS = {
                                  ctypes.c_size_t, _P]),
     "moe_dispatch": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P,
                                     ctypes.POINTER(moe_stats), _P, ctypes.c_size_t, _P]),
-    "moe_expert_ffn": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+    "moe_expert_ffn": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                       ctypes.c_size_t, _P]),
     "moe_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P]),
     "moe_forward": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    ctypes.POINTER(moe_stats), _P, ctypes.c_size_t, _P,
                                    ctypes.POINTER(moe_timing)]),
     "moe_device_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
+    "moe_kernel_launches": (ctypes.c_int64, []),
 }
 
 
@@ -187,10 +188,10 @@ def moe_dispatch(cfg, topk_idx, probs, x, final_idx, pos, offsets, perm, x_perm,
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
-def moe_expert_ffn(cfg, x, x_perm, offsets, w_gate, w_up, w_down, b1, b2, y_perm,
+def moe_expert_ffn(cfg, x, x_perm, offsets, counts, w_gate, w_up, w_down, b1, b2, y_perm,
                    workspace=None, stream=None) -> int:
     return _check("moe_expert_ffn", lib().moe_expert_ffn(
-        ctypes.byref(cfg), _ptr(x), _ptr(x_perm), _ptr(offsets), _ptr(w_gate), _ptr(w_up),
+        ctypes.byref(cfg), _ptr(x), _ptr(x_perm), _ptr(offsets), _ptr(counts), _ptr(w_gate), _ptr(w_up),
         _ptr(w_down), _ptr(b1), _ptr(b2), _ptr(y_perm), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
@@ -216,6 +217,10 @@ def moe_device_status(workspace, stream=None) -> int:
     _check("moe_device_status", lib().moe_device_status(_ptr(workspace), _stream(stream),
                                                         ctypes.byref(out)))
     return out.value
+
+
+def moe_kernel_launches() -> int:
+    return lib().moe_kernel_launches()
 
 
 def alloc_workspace(cfg, device="cuda"):

@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -22,7 +23,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Layout {
   size_t status, acc_p, acc_pick, ticket, zero_end;  // [status .. zero_end) is cleared per call
-  size_t topk_idx, topk_w, probs, final_idx, slot, pos, offsets, perm;
+  size_t topk_idx, topk_w, probs, final_idx, slot, pos, offsets, counts, perm;
   size_t part, chunk_cnt, local_rank, rr_state, rr_scratch;
   size_t x_perm, h, y_perm, total;
 };
@@ -54,6 +55,7 @@ Layout layout_of(const moe_config* c) {
   L.slot = take(N * k * 4);
   L.pos = take(N * k * 4);
   L.offsets = take((E + c->n_shared + 1) * 4);
+  L.counts = take(E * 4);
   L.perm = take((size_t)max_rows_of(c) * 4);
   L.part = take((size_t)rs.ks * N * E * 4);
   L.chunk_cnt = take(chunks * E * 4);
@@ -136,12 +138,14 @@ int dispatch_impl(const moe_config* c, const int32_t* topk_idx, const float* pro
 }
 
 int ffn_impl(const moe_config* c, const void* x, const void* x_perm, const int32_t* offsets,
-             const void* w_gate, const void* w_up, const void* w_down, const void* b1,
-             const void* b2, void* y_perm, void* ws, cudaStream_t s, cudaEvent_t mid) {
+             const int32_t* counts, const void* w_gate, const void* w_up, const void* w_down,
+             const void* b1, const void* b2, void* y_perm, void* ws, cudaStream_t s,
+             cudaEvent_t mid) {
   const Layout L = layout_of(c);
   FfnParams fp{};
   fp.N = c->n_tokens; fp.d = c->d_model; fp.F = c->d_ff; fp.E = c->n_experts;
-  fp.S = c->n_shared; fp.act = c->act; fp.offsets = offsets; fp.x = x; fp.x_perm = x_perm;
+  fp.S = c->n_shared; fp.k = c->top_k; fp.act = c->act; fp.offsets = offsets; fp.counts = counts;
+  fp.x = x; fp.x_perm = x_perm;
   fp.w_gate = w_gate; fp.w_up = w_up; fp.w_down = w_down;
   fp.b1 = c->has_ffn_bias ? b1 : nullptr; fp.b2 = c->has_ffn_bias ? b2 : nullptr;
   fp.h = at<void>(ws, L.h); fp.y_perm = y_perm;
@@ -163,9 +167,18 @@ int combine_impl(const moe_config* c, const void* y_perm, const int32_t* offsets
 }  // namespace
 }  // namespace moe
 
+namespace moe {
+namespace {
+std::atomic<long long> g_launches{0};
+}  // namespace
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace moe
+
 using namespace moe;
 
 extern "C" {
+
+int64_t moe_kernel_launches(void) { return (int64_t)g_launches.load(std::memory_order_relaxed); }
 
 const char* moe_status_string(int st) {
   switch (st) {
@@ -267,8 +280,9 @@ int moe_dispatch(const moe_config* c, const int32_t* topk_idx, const float* prob
 }
 
 int moe_expert_ffn(const moe_config* c, const void* x, const void* x_perm, const int32_t* offsets,
-                   const void* w_gate, const void* w_up, const void* w_down, const void* b1,
-                   const void* b2, void* y_perm, void* ws, size_t ws_bytes, void* stream) {
+                   const int32_t* counts, const void* w_gate, const void* w_up,
+                   const void* w_down, const void* b1, const void* b2, void* y_perm, void* ws,
+                   size_t ws_bytes, void* stream) {
   int st = moe_validate_config(c);
   if (st != MOE_OK) return st;
   if ((st = check_ws(c, ws, ws_bytes)) != MOE_OK) return st;
@@ -279,7 +293,7 @@ int moe_expert_ffn(const moe_config* c, const void* x, const void* x_perm, const
       !aligned16(y_perm) || (w_up && !aligned16(w_up)))
     return MOE_ERR_INVALID_ARG;
   if (c->n_tokens == 0) return MOE_OK;
-  return ffn_impl(c, x, x_perm, offsets, w_gate, w_up, w_down, b1, b2, y_perm, ws,
+  return ffn_impl(c, x, x_perm, offsets, counts, w_gate, w_up, w_down, b1, b2, y_perm, ws,
                   static_cast<cudaStream_t>(stream), nullptr);
 }
 
@@ -319,13 +333,17 @@ int moe_forward(const moe_config* c, const void* x, const void* w_router, const 
                   probs, stats, ws, s);
   if (st != MOE_OK) return st;
   record(timing, 1, s);
+  // the expert GEMMs read the per-expert counts: the caller's array when given
+  moe_stats st_fwd{};
+  if (stats) st_fwd = *stats;
+  if (!st_fwd.counts) st_fwd.counts = at<int32_t>(ws, L.counts);
   st = dispatch_impl(c, at<int32_t>(ws, L.topk_idx), probs, x, at<int32_t>(ws, L.final_idx),
                      at<int32_t>(ws, L.pos), at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.perm),
-                     at<void>(ws, L.x_perm), stats, ws, s);
+                     at<void>(ws, L.x_perm), &st_fwd, ws, s);
   if (st != MOE_OK) return st;
   record(timing, 2, s);
-  st = ffn_impl(c, x, at<void>(ws, L.x_perm), at<int32_t>(ws, L.offsets), w_gate, w_up, w_down,
-                b1, b2, at<void>(ws, L.y_perm), ws, s,
+  st = ffn_impl(c, x, at<void>(ws, L.x_perm), at<int32_t>(ws, L.offsets), st_fwd.counts, w_gate,
+                w_up, w_down, b1, b2, at<void>(ws, L.y_perm), ws, s,
                 timing ? static_cast<cudaEvent_t>(timing->events[3]) : nullptr);
   if (st != MOE_OK) return st;
   record(timing, 4, s);

@@ -69,12 +69,22 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
     float acc[VN];
 #pragma unroll
     for (int q = 0; q < VN; ++q) acc[q] = 0.f;
-    for (int r = 0; r < n; ++r) {
-      float f[VN];
-      Vec<T>::load(src[(size_t)rows[r] * nvec + v], f);
-      const float g = gates[r];
+    // rows in groups of 4: the loads of a group are issued before its FMAs
+    for (int r0 = 0; r0 < n; r0 += 4) {
+      uint4 u[4];
 #pragma unroll
-      for (int q = 0; q < VN; ++q) acc[q] = fmaf(g, f[q], acc[q]);
+      for (int i = 0; i < 4; ++i)
+        if (r0 + i < n) u[i] = src[(size_t)rows[r0 + i] * nvec + v];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (r0 + i < n) {
+          float f[VN];
+          Vec<T>::load(u[i], f);
+          const float g = gates[r0 + i];
+#pragma unroll
+          for (int q = 0; q < VN; ++q) acc[q] = fmaf(g, f[q], acc[q]);
+        }
+      }
     }
     dst[(size_t)t * nvec + v] = Vec<T>::store(acc);
   }
@@ -86,8 +96,8 @@ cudaError_t launch_combine(const CombineParams& p, bool bf16, cudaStream_t s) {
   const int vn = bf16 ? 8 : 4;
   const int nvec = p.d / vn;
   int threads = nvec < 256 ? ((nvec + 31) / 32) * 32 : 256;
-  if (bf16) combine_kernel<__nv_bfloat16><<<p.N, threads, 0, s>>>(p);
-  else combine_kernel<float><<<p.N, threads, 0, s>>>(p);
+  if (bf16) { combine_kernel<__nv_bfloat16><<<p.N, threads, 0, s>>>(p); count_launch(); }
+  else { combine_kernel<float><<<p.N, threads, 0, s>>>(p); count_launch(); }
   return cudaGetLastError();
 }
 

@@ -406,9 +406,11 @@ size_t reroute_scratch_ints(int N, int k, int E) {
 cudaError_t launch_dispatch(const DispatchParams& p, bool bf16, cudaStream_t s) {
   const int W = kRankTC / 32;
   dispatch_rank_kernel<<<p.n_chunks, kRankTC, sizeof(uint32_t) * p.E * W, s>>>(p);
+  count_launch();
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   dispatch_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+  count_launch();
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (p.cap_mode == 2) {
@@ -428,9 +430,10 @@ cudaError_t launch_dispatch(const DispatchParams& p, bool bf16, cudaStream_t s) 
     err = cudaLaunchCooperativeKernel((const void*)dispatch_reroute_kernel, dim3(grid),
                                       dim3(kRrThreads), args, 0, s);
     if (err != cudaSuccess) return err;
+    count_launch();
   }
-  if (bf16) dispatch_scatter_kernel<__nv_bfloat16><<<p.N, 128, 0, s>>>(p);
-  else dispatch_scatter_kernel<float><<<p.N, 128, 0, s>>>(p);
+  if (bf16) { dispatch_scatter_kernel<__nv_bfloat16><<<p.N, 128, 0, s>>>(p); count_launch(); }
+  else { dispatch_scatter_kernel<float><<<p.N, 128, 0, s>>>(p); count_launch(); }
   return cudaGetLastError();
 }
 

@@ -129,12 +129,13 @@ __global__ void __launch_bounds__(256) ffn_simt_kernel(FfnParams p) {
 cudaError_t launch_ffn_simt(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) {
   const int mt = (int)((p.max_total_rows + kBM - 1) / kBM);
   dim3 g1(mt, (p.F + kBN - 1) / kBN), g2(mt, (p.d + kBN - 1) / kBN);
-  if (p.act == 1) ffn_simt_kernel<1, true><<<g1, 256, 0, s>>>(p);
-  else ffn_simt_kernel<1, false><<<g1, 256, 0, s>>>(p);
+  if (p.act == 1) { ffn_simt_kernel<1, true><<<g1, 256, 0, s>>>(p); count_launch(); }
+  else { ffn_simt_kernel<1, false><<<g1, 256, 0, s>>>(p); count_launch(); }
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (mid) cudaEventRecord(mid, s);
   ffn_simt_kernel<2, false><<<g2, 256, 0, s>>>(p);
+  count_launch();
   return cudaGetLastError();
 }
 

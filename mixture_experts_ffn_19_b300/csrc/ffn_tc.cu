@@ -238,6 +238,255 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ 
   }
 }
 
+// ---------------------------------------------------------------- swap-AB variant
+//
+// For decode-sized batches (a few tokens per expert) the 128-row token tiles
+// above are mostly padding.  Here the roles swap: the weights are the MMA's
+// M=128 operand and the expert's tokens (in chunks of up to 64) are the N
+// operand, N = tokens rounded up to 16.  GEMM-1 stacks 64 gate rows over 64 up
+// rows of the same features in one M=128 tile; the epilogue warps holding the
+// up rows pass them through shared memory to the warps holding the gate rows,
+// which form silu(g)*u and store H.  GEMM-2 takes 128 rows of W_down per tile.
+// Tiles walk segment by segment, feature block by feature block, token chunk
+// fastest, so a weight tile is read from HBM once.
+
+namespace swp {
+
+constexpr int BM = 128, TOK = 64, BK = 64;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = TOK * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int STAGES = 8;
+constexpr int TMEM_COLS = 128;                 // two 64-column accumulators
+constexpr int XS = TOK + 1;                    // exchange row (floats), conflict-free
+
+struct Ctrl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t xfull;                // up values written to the exchange buffer
+  uint64_t xempty;               // exchange buffer consumed
+  uint32_t tmem_base;
+  int abort;
+  int total_chunks;
+  int pad;
+  int ch_prefix[kMaxExperts + 16];
+};
+
+constexpr size_t XCH_BYTES = (size_t)64 * XS * 4;
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + XCH_BYTES + sizeof(Ctrl);
+
+struct Params {
+  int E, S, N, K, n_out, n_fb;   // n_fb: feature blocks per segment
+  const int32_t* offsets;
+  const int32_t* counts;         // [E] valid rows of the routed segments
+  __nv_bfloat16* out;
+  int* status;
+};
+
+__device__ __forceinline__ int seg_rows(const Params& p, int s) {
+  return s < p.E ? p.counts[s] : p.N;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                   const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                   Params p) {
+  // tmB0/tmB1: token rows (x_perm / x for GEMM-1, H for GEMM-2);
+  // tmA0/tmA1: weights (gate / up for GEMM-1, down for GEMM-2)
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  float* xch = reinterpret_cast<float*>(smem + (size_t)STAGES * STAGE_BYTES);
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + (size_t)STAGES * STAGE_BYTES + XCH_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nseg = p.E + p.S;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) { mbar_init(&ctrl->full[s], 1); mbar_init(&ctrl->empty[s], 1); }
+    for (int b = 0; b < 2; ++b) { mbar_init(&ctrl->tfull[b], 1); mbar_init(&ctrl->tempty[b], 128); }
+    mbar_init(&ctrl->xfull, 64);
+    mbar_init(&ctrl->xempty, 64);
+    ctrl->abort = 0;
+    int run = 0;
+    for (int s = 0; s < nseg; ++s) {
+      ctrl->ch_prefix[s] = run;
+      run += (seg_rows(p, s) + TOK - 1) / TOK;
+    }
+    ctrl->ch_prefix[nseg] = run;
+    ctrl->total_chunks = run;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA0); tma_prefetch_desc(&tmA1);
+    tma_prefetch_desc(&tmB0); tma_prefetch_desc(&tmB1);
+  }
+  if (warp == 1) { tmem_alloc(&ctrl->tmem_base, TMEM_COLS); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctrl->tmem_base;
+  const int total_tiles = ctrl->total_chunks * p.n_fb;
+  const int KB = (p.K + BK - 1) / BK;
+  volatile int* abort = &ctrl->abort;
+  const Ctrl* cc = ctrl;
+  // tile -> (segment, feature block, token chunk); chunk fastest
+  auto coord = [&](int T, int& seg, int& fb, int& ch) {
+    const int q = T / p.n_fb;
+    int lo = 0, hi = nseg - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cc->ch_prefix[mid] <= q) lo = mid; else hi = mid - 1;
+    }
+    const int nch = cc->ch_prefix[lo + 1] - cc->ch_prefix[lo];
+    const int local = T - cc->ch_prefix[lo] * p.n_fb;
+    seg = lo; fb = local / nch; ch = local % nch;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t kc = 0;
+      for (int T = blockIdx.x; T < total_tiles && !*abort; T += gridDim.x) {
+        int seg, fb, ch;
+        coord(T, seg, fb, ch);
+        const CUtensorMap* bmap = &tmB0;
+        int b_row = p.offsets[seg] + ch * TOK;
+        if (MODE == 0 && seg >= p.E) { bmap = &tmB1; b_row = ch * TOK; }
+        const int a_row = seg * p.n_out + fb * (MODE == 0 ? BM / 2 : BM);
+        for (int kb = 0; kb < KB; ++kb, ++kc) {
+          const int st = kc % STAGES;
+          const uint32_t ph = (kc / STAGES) & 1;
+          if (!mbar_wait(&ctrl->empty[st], ph ^ 1, abort, p.status)) break;
+          uint8_t* a_s = smem + (size_t)st * STAGE_BYTES;
+          mbar_arrive_expect_tx(&ctrl->full[st], STAGE_BYTES);
+          if (MODE == 0) {
+            tma_load_2d(a_s, &tmA0, &ctrl->full[st], kb * BK, a_row);
+            tma_load_2d(a_s + A_BYTES / 2, &tmA1, &ctrl->full[st], kb * BK, a_row);
+          } else {
+            tma_load_2d(a_s, &tmA0, &ctrl->full[st], kb * BK, a_row);
+          }
+          tma_load_2d(a_s + A_BYTES, bmap, &ctrl->full[st], kb * BK, b_row);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t kc = 0, it = 0;
+      for (int T = blockIdx.x; T < total_tiles && !*abort; T += gridDim.x, ++it) {
+        int seg, fb, ch;
+        coord(T, seg, fb, ch);
+        const int nt = min(TOK, seg_rows(p, seg) - ch * TOK);
+        const uint32_t idesc = idesc_bf16_f32(BM, (nt + 15) / 16 * 16);
+        const uint32_t buf = it & 1, use = it >> 1;
+        if (!mbar_wait(&ctrl->tempty[buf], (use & 1) ^ 1, abort, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * TOK;
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb, ++kc) {
+          const int st = kc % STAGES;
+          const uint32_t ph = (kc / STAGES) & 1;
+          if (!mbar_wait(&ctrl->full[st], ph, abort, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + (size_t)st * STAGE_BYTES);
+          const uint64_t adesc = sdesc_kmajor_sw128(a_addr);
+          const uint64_t bdesc = sdesc_kmajor_sw128(a_addr + A_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            umma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+          umma_commit(&ctrl->empty[st]);
+        }
+        if (!ok) break;
+        umma_commit(&ctrl->tfull[buf]);
+      }
+    }
+  } else {
+    const int q = warp & 3;                      // TMEM lanes 32q .. 32q+31 = weight rows
+    uint32_t it = 0;
+    for (int T = blockIdx.x; T < total_tiles; T += gridDim.x, ++it) {
+      if (__any_sync(0xffffffffu, *abort != 0)) break;
+      int seg, fb, ch;
+      coord(T, seg, fb, ch);
+      const int nt = min(TOK, seg_rows(p, seg) - ch * TOK);
+      const uint32_t buf = it & 1, use = it >> 1;
+      const bool ok = mbar_wait(&ctrl->tfull[buf], use & 1, abort, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * TOK;
+      const int row0 = p.offsets[seg] + ch * TOK;
+      const int ncc = (nt + 31) / 32;
+      if (MODE == 0) {
+        // rows 64..127 (q = 2, 3) hold x.Wu; rows 0..63 (q = 0, 1) hold x.Wg
+        // The hand-over uses two mbarriers (bounded waits), not a named
+        // barrier, so a warp that gives up cannot strand the others.
+        const int f = (q & 1) * 32 + lane;       // feature inside the 64-wide block
+        bool xok = true;
+        if (q >= 2) {
+          xok = mbar_wait(&ctrl->xempty, (it & 1) ^ 1, abort, p.status);
+          if (__all_sync(0xffffffffu, xok)) {
+            for (int c = 0; c < ncc; ++c) {
+              uint32_t u[32];
+              tmem_ld32(taddr + c * 32, u);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) xch[f * XS + c * 32 + i] = __uint_as_float(u[i]);
+            }
+            mbar_arrive(&ctrl->xfull);
+          }
+        } else {
+          xok = mbar_wait(&ctrl->xfull, it & 1, abort, p.status);
+        }
+        if (!__all_sync(0xffffffffu, xok)) break;
+        if (q < 2) {
+          const int col = fb * 64 + f;
+          for (int c = 0; c < ncc; ++c) {
+            uint32_t g[32];
+            tmem_ld32(taddr + c * 32, g);
+            tmem_wait_ld();
+            if (col < p.n_out) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const int t = c * 32 + i;
+                if (t < nt) {
+                  const float h = silu_f(__uint_as_float(g[i])) * xch[f * XS + t];
+                  p.out[(size_t)(row0 + t) * p.n_out + col] = __float2bfloat16_rn(h);
+                }
+              }
+            }
+          }
+          mbar_arrive(&ctrl->xempty);            // the next tile may overwrite xch
+        }
+      } else {
+        const int col = fb * BM + q * 32 + lane;
+        for (int c = 0; c < ncc; ++c) {
+          uint32_t y[32];
+          tmem_ld32(taddr + c * 32, y);
+          tmem_wait_ld();
+          if (col < p.n_out) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int t = c * 32 + i;
+              if (t < nt) p.out[(size_t)(row0 + t) * p.n_out + col] = __float2bfloat16_rn(__uint_as_float(y[i]));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&ctrl->tempty[buf]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace swp
+
 // ---------------------------------------------------------------- host side
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -269,9 +518,52 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 
 }  // namespace
 
+namespace {
+
+// Swap-AB (weights as the M operand) when experts see few tokens: decode-sized
+// batches, where 128-row token tiles would be mostly padding.
+bool use_swap(const FfnParams& p) {
+  if (!p.counts) return false;
+  if ((int64_t)p.N * p.k > 64LL * p.E) return false;
+  return p.S == 0 || p.N <= 512;
+}
+
+cudaError_t launch_swap(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) {
+  cudaError_t err = cudaFuncSetAttribute(swp::ffn_tc_swap_kernel<0>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)swp::SMEM_BYTES);
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(swp::ffn_tc_swap_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)swp::SMEM_BYTES);
+  if (err != cudaSuccess) return err;
+  const int ET = p.E + p.S;
+  CUtensorMap b0, b1, a0, a1;
+  if (!make_map(&b0, p.x_perm, (uint64_t)p.max_rows, p.d, swp::TOK) ||
+      !make_map(&b1, p.x, (uint64_t)p.N, p.d, swp::TOK) ||
+      !make_map(&a0, p.w_gate, (uint64_t)ET * p.F, p.d, swp::BM / 2) ||
+      !make_map(&a1, p.w_up, (uint64_t)ET * p.F, p.d, swp::BM / 2))
+    return cudaErrorInvalidValue;
+  swp::Params t1{p.E, p.S, p.N, p.d, p.F, (p.F + 63) / 64, p.offsets, p.counts,
+            static_cast<__nv_bfloat16*>(p.h), p.status};
+  swp::ffn_tc_swap_kernel<0><<<p.num_sms, NUM_THREADS, swp::SMEM_BYTES, s>>>(b0, b1, a0, a1, t1);
+  count_launch();
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (mid) cudaEventRecord(mid, s);
+  if (!make_map(&b0, p.h, (uint64_t)p.max_total_rows, p.F, swp::TOK) ||
+      !make_map(&a0, p.w_down, (uint64_t)ET * p.d, p.F, swp::BM))
+    return cudaErrorInvalidValue;
+  swp::Params t2{p.E, p.S, p.N, p.F, p.d, (p.d + swp::BM - 1) / swp::BM, p.offsets, p.counts,
+            static_cast<__nv_bfloat16*>(p.y_perm), p.status};
+  swp::ffn_tc_swap_kernel<1><<<p.num_sms, NUM_THREADS, swp::SMEM_BYTES, s>>>(b0, b0, a0, a0, t2);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_ffn_tc(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) {
   cudaError_t err = get_encoder();
   if (err != cudaSuccess) return err;
+  if (use_swap(p)) return launch_swap(p, s, mid);
   err = cudaFuncSetAttribute(ffn_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES);
   if (err != cudaSuccess) return err;
@@ -289,6 +581,7 @@ cudaError_t launch_ffn_tc(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) {
   TcParams t1{p.E, p.S, p.d, p.F, (p.F + BN / 2 - 1) / (BN / 2), BN / 2, p.offsets,
               static_cast<__nv_bfloat16*>(p.h), p.status};
   ffn_tc_kernel<0><<<p.num_sms, NUM_THREADS, SMEM_BYTES, s>>>(a0, a1, b0, b1, t1);
+  count_launch();
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (mid) cudaEventRecord(mid, s);
@@ -299,6 +592,7 @@ cudaError_t launch_ffn_tc(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) {
   TcParams t2{p.E, p.S, p.F, p.d, (p.d + BN - 1) / BN, BN, p.offsets,
               static_cast<__nv_bfloat16*>(p.y_perm), p.status};
   ffn_tc_kernel<1><<<p.num_sms, NUM_THREADS, SMEM_BYTES, s>>>(a0, a0, b0, b0, t2);
+  count_launch();
   return cudaGetLastError();
 }
 

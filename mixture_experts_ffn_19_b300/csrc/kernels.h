@@ -82,8 +82,9 @@ struct DispatchParams {
 };
 
 struct FfnParams {
-  int N, d, F, E, S, act;
+  int N, d, F, E, S, k, act;
   const int32_t* offsets;    // [E+S+1]
+  const int32_t* counts;     // [E] valid rows of the routed segments, or null
   const void* x;             // [N, d]
   const void* x_perm;        // [max_rows, d]
   const void* w_gate;        // [E+S, F, d]
@@ -107,6 +108,9 @@ struct CombineParams {
   const float* topk_w;
   void* y;
 };
+
+// Kernels this library has launched in this process (host-side count).
+void count_launch();
 
 cudaError_t launch_route(const RouteParams& p, bool bf16, cudaStream_t s);
 cudaError_t launch_dispatch(const DispatchParams& p, bool bf16, cudaStream_t s);

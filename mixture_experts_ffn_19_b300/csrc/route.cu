@@ -247,12 +247,14 @@ cudaError_t launch_simt_t(const RouteParams& p, const RouteSplit& sp, cudaStream
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   kern<<<dim3((p.N + kTM - 1) / kTM, sp.ks), kThreads, smem, s>>>(p, sp);
+  count_launch();
   return cudaGetLastError();
 }
 
 template <int EJ>
 cudaError_t launch_finish_t(const RouteParams& p, const RouteSplit& sp, cudaStream_t s) {
   route_finish_kernel<EJ><<<route_finish_blocks(p.N), kThreads, 0, s>>>(p, sp);
+  count_launch();
   return cudaGetLastError();
 }
 
@@ -285,8 +287,11 @@ RouteSplit route_split(int N, int d, bool bf16) {
   const int tile = bf16 ? 128 : kTM;
   const int tiles = N > 0 ? (N + tile - 1) / tile : 1;
   const int kblocks = (d + 63) / 64;
-  int ks = (2 * 148 + tiles - 1) / tiles;
-  ks = ks < 1 ? 1 : (ks > kblocks ? kblocks : ks);
+  // about one CTA per SM, at most 16 slices (each slice is one more partial
+  // per logit to read back)
+  int ks = (148 + tiles - 1) / tiles;
+  ks = ks < 1 ? 1 : (ks > 16 ? 16 : ks);
+  ks = ks > kblocks ? kblocks : ks;
   const int k_slice = (kblocks + ks - 1) / ks * 64;
   RouteSplit r;
   r.k_slice = k_slice;
@@ -306,6 +311,7 @@ cudaError_t launch_route(const RouteParams& p, bool bf16, cudaStream_t s) {
   if (sp.ks > 1) {
     const size_t n = (size_t)p.N * p.E;
     route_reduce_kernel<<<(unsigned)((n + kThreads - 1) / kThreads), kThreads, 0, s>>>(p.part, sp.ks, n);
+    count_launch();
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   MOE_EJ_SWITCH(p.E, launch_finish_t, p, sp, s)

@@ -184,6 +184,7 @@ cudaError_t launch_route_logits_tc(const RouteSplit& s, const void* x, const voi
   if (err != cudaSuccess) return err;
   dim3 grid((N + BM - 1) / BM, s.ks);
   route_logits_tc<<<grid, NUM_THREADS, smem, stream>>>(mx, mw, p);
+  count_launch();
   return cudaGetLastError();
 }
 

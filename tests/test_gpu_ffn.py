@@ -36,7 +36,7 @@ def oracle_routing(w, inp):
     return r, d
 
 
-def run_ffn(w, inp, members, device):
+def run_ffn(w, inp, members, device, with_counts=True):
     cfg = config_of(w)
     ws = moe.alloc_workspace(cfg, device)
     offsets = host_layout(w, members)
@@ -47,7 +47,8 @@ def run_ffn(w, inp, members, device):
         xp[offsets[e]:offsets[e] + len(m)] = x[m]
     xd = to_dev(x)
     y_perm = torch.zeros((RT, w.d_model), dtype=xd.dtype, device=device)
-    moe.moe_expert_ffn(cfg, xd, to_dev(xp), to_dev(offsets), to_dev(inp["w_gate"]),
+    counts = to_dev(np.array([len(m) for m in members], dtype=np.int32)) if with_counts else None
+    moe.moe_expert_ffn(cfg, xd, to_dev(xp), to_dev(offsets), counts, to_dev(inp["w_gate"]),
                        to_dev(inp["w_up"]), to_dev(inp["w_down"]), to_dev(inp["b1"]),
                        to_dev(inp["b2"]), y_perm, ws)
     assert moe.moe_device_status(ws) == moe.MOE_OK
@@ -75,14 +76,21 @@ CASES = [
     synth.small_workload("tiny_fp32", n_tokens=100, d_model=72, n_experts=5, top_k=3, d_ff=136),
     synth.small_workload("tiny_fp32", n_tokens=90, d_model=64, n_experts=4, top_k=2, d_ff=96,
                          act=synth.ACT_SWIGLU, has_ffn_bias=False, n_shared=1),
+    # decode-sized batches: few tokens per expert (weights-as-M variant)
+    synth.small_workload("decode_dsv2", d_model=256, d_ff=320),
+    synth.small_workload("decode_mixtral", d_model=512, d_ff=1024),
+    synth.small_workload("decode_mixtral", n_tokens=200, d_model=192, top_k=1, d_ff=200),
+    synth.small_workload("decode_dsv2", n_tokens=300, d_model=128, n_experts=64, top_k=2,
+                         d_ff=136, n_shared=1),
 ]
 
 
+@pytest.mark.parametrize("with_counts", [True, False], ids=["counts", "nocounts"])
 @pytest.mark.parametrize("w", CASES, ids=lambda w: f"{w.name}-N{w.n_tokens}-d{w.d_model}-E{w.n_experts}-F{w.d_ff}")
-def test_expert_ffn(cuda, w):
+def test_expert_ffn(cuda, w, with_counts):
     inp = synth.make_inputs(w)
     _, dsp = oracle_routing(w, inp)
-    offsets, y = run_ffn(w, inp, dsp["members"], cuda)
+    offsets, y = run_ffn(w, inp, dsp["members"], cuda, with_counts)
     x = oracle.widen(inp["x"])
     worst = 0.0
     for e, m in enumerate(dsp["members"]):
