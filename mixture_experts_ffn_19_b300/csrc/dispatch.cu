@@ -126,7 +126,7 @@ __device__ void write_layout(const DispatchParams& p, const int* fill, int n_dro
 }
 
 __global__ void __launch_bounds__(kPlanThreads) dispatch_plan_kernel(DispatchParams p) {
-  const int E = p.E, k = p.k, N = p.N, C = p.C;
+  const int E = p.E, C = p.C;
   __shared__ int fill[kMaxExperts], total[kMaxExperts];
   __shared__ int warp_tot[kPlanThreads / 32];
   __shared__ int s_total;

@@ -33,31 +33,45 @@ namespace moe {
 
 namespace {
 
-constexpr int BM = 128, BK = 64, BN = 256;
-constexpr int STAGES = 4;
+constexpr int BM = 128, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
-constexpr int TMEM_COLS = 512;
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 
-struct Ctrl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
-  uint32_t tmem_base;
-  int abort;
-  int total_mtiles;
-  int pad;
-  int mt_prefix[kMaxExperts + 16];
+// Tile width BN (the MMA's N: output columns of a GEMM-2 tile, gate + up
+// columns of a GEMM-1 tile) and the depth of the shared-memory ring.
+#ifndef MOE_PREFILL_BN
+#define MOE_PREFILL_BN 256
+#endif
+#ifndef MOE_PREFILL_STAGES
+#define MOE_PREFILL_STAGES 4
+#endif
+
+template <int BN_, int STAGES_>
+struct TileCfg {
+  static constexpr int BN = BN_, STAGES = STAGES_;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN;       // two accumulators
+  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+  struct Ctrl {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint32_t tmem_base;
+    int abort;
+    int total_mtiles;
+    int pad;
+    int mt_prefix[kMaxExperts + 16];
+  };
+  static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctrl);
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+  static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "tmem");
 };
-
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctrl);
+using Prefill = TileCfg<MOE_PREFILL_BN, MOE_PREFILL_STAGES>;
 
 struct TcParams {
-  int E, S, K, n_out, n_tiles_n, bn_out;  // bn_out: output columns per tile (128 or 256)
+  int E, S, K, n_out, n_tiles_n, bn_out;  // bn_out: output columns per tile
   const int32_t* offsets;
   __nv_bfloat16* out;
   int* status;
@@ -67,7 +81,8 @@ struct TileCoord {
   int seg, m, n;
 };
 
-__device__ __forceinline__ TileCoord tile_coord(const Ctrl* c, int nseg, int n_tiles_n, int T) {
+template <class CtrlT>
+__device__ __forceinline__ TileCoord tile_coord(const CtrlT* c, int nseg, int n_tiles_n, int T) {
   const int q = T / n_tiles_n;
   int lo = 0, hi = nseg - 1;
   while (lo < hi) {   // largest segment whose first row tile is <= q
@@ -81,11 +96,15 @@ __device__ __forceinline__ TileCoord tile_coord(const Ctrl* c, int nseg, int n_t
 
 __device__ __forceinline__ float silu_f(float a) { return a / (1.f + __expf(-a)); }
 
-template <int MODE>
+template <int MODE, class C>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
               const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
               TcParams p) {
+  constexpr int BN = C::BN, STAGES = C::STAGES, B_BYTES = C::B_BYTES;
+  constexpr int STAGE_BYTES = C::STAGE_BYTES, TMEM_COLS = C::TMEM_COLS;
+  constexpr uint32_t IDESC = C::IDESC;
+  using Ctrl = typename C::Ctrl;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -188,10 +207,10 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ 
       const int col0 = tc.n * p.bn_out;
       if (MODE == 0) {
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < BN / 64; ++c) {
           uint32_t g[32], u[32];
           tmem_ld32(taddr + c * 32, g);
-          tmem_ld32(taddr + 128 + c * 32, u);
+          tmem_ld32(taddr + BN / 2 + c * 32, u);
           tmem_wait_ld();
           uint32_t packed[16];
 #pragma unroll
@@ -209,7 +228,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ 
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < BN / 32; ++c) {
           uint32_t a[32];
           tmem_ld32(taddr + c * 32, a);
           tmem_wait_ld();
@@ -560,15 +579,16 @@ cudaError_t launch_swap(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) {
 
 }  // namespace
 
-cudaError_t launch_ffn_tc(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) {
-  cudaError_t err = get_encoder();
+namespace {
+
+template <class C>
+cudaError_t launch_prefill(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) {
+  constexpr int BN = C::BN;
+  cudaError_t err = cudaFuncSetAttribute(ffn_tc_kernel<0, C>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
   if (err != cudaSuccess) return err;
-  if (use_swap(p)) return launch_swap(p, s, mid);
-  err = cudaFuncSetAttribute(ffn_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SMEM_BYTES);
-  if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(ffn_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SMEM_BYTES);
+  err = cudaFuncSetAttribute(ffn_tc_kernel<1, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::SMEM_BYTES);
   if (err != cudaSuccess) return err;
   const int ET = p.E + p.S;
   CUtensorMap a0, a1, b0, b1;
@@ -580,10 +600,9 @@ cudaError_t launch_ffn_tc(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) {
     return cudaErrorInvalidValue;
   TcParams t1{p.E, p.S, p.d, p.F, (p.F + BN / 2 - 1) / (BN / 2), BN / 2, p.offsets,
               static_cast<__nv_bfloat16*>(p.h), p.status};
-  ffn_tc_kernel<0><<<p.num_sms, NUM_THREADS, SMEM_BYTES, s>>>(a0, a1, b0, b1, t1);
+  ffn_tc_kernel<0, C><<<p.num_sms, NUM_THREADS, C::SMEM_BYTES, s>>>(a0, a1, b0, b1, t1);
   count_launch();
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
   if (mid) cudaEventRecord(mid, s);
   // GEMM-2: A = H, B = down weights
   if (!make_map(&a0, p.h, (uint64_t)p.max_total_rows, p.F, BM) ||
@@ -591,9 +610,18 @@ cudaError_t launch_ffn_tc(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) {
     return cudaErrorInvalidValue;
   TcParams t2{p.E, p.S, p.F, p.d, (p.d + BN - 1) / BN, BN, p.offsets,
               static_cast<__nv_bfloat16*>(p.y_perm), p.status};
-  ffn_tc_kernel<1><<<p.num_sms, NUM_THREADS, SMEM_BYTES, s>>>(a0, a0, b0, b0, t2);
+  ffn_tc_kernel<1, C><<<p.num_sms, NUM_THREADS, C::SMEM_BYTES, s>>>(a0, a0, b0, b0, t2);
   count_launch();
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_tc(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) {
+  cudaError_t err = get_encoder();
+  if (err != cudaSuccess) return err;
+  if (use_swap(p)) return launch_swap(p, s, mid);
+  return launch_prefill<Prefill>(p, s, mid);
 }
 
 }  // namespace moe
