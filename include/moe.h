@@ -196,7 +196,8 @@ int moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const float* pr
  *   counts  [E]      in, nullable: kept rows per routed expert (stats->counts
  *           of moe_dispatch).  With counts, batches with few tokens per expert
  *           run a variant with the weights as the wide MMA operand; without,
- *           every padded row of every segment is computed (same results)
+ *           every padded row of every segment is computed (the same sums up to
+ *           fp32 summation order)
  *   w_gate  [E+S, F, d]  SwiGLU gate weight | GELU W1
  *   w_up    [E+S, F, d]  SwiGLU up weight   | GELU: NULL
  *   w_down  [E+S, d, F]  down weight (W2)

@@ -76,6 +76,10 @@ CASES = [
     synth.small_workload("tiny_fp32", n_tokens=100, d_model=72, n_experts=5, top_k=3, d_ff=136),
     synth.small_workload("tiny_fp32", n_tokens=90, d_model=64, n_experts=4, top_k=2, d_ff=96,
                          act=synth.ACT_SWIGLU, has_ffn_bias=False, n_shared=1),
+    # many rows per expert: odd row-tile counts, shared expert,
+    # K and N tails
+    synth.small_workload("mixtral_prefill", n_tokens=1100, d_model=256, n_experts=2, top_k=2, d_ff=384),
+    synth.small_workload("dsv2", n_tokens=800, d_model=200, n_experts=2, top_k=2, d_ff=136, n_shared=1),
     # decode-sized batches: few tokens per expert (weights-as-M variant)
     synth.small_workload("decode_dsv2", d_model=256, d_ff=320),
     synth.small_workload("decode_mixtral", d_model=512, d_ff=1024),

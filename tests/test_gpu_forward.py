@@ -79,6 +79,8 @@ SMALL = [
     synth.small_workload("dsv2", n_tokens=400, d_model=320, n_experts=20, top_k=6, d_ff=192),
     synth.small_workload("e64_reroute", n_tokens=2048, d_model=256, d_ff=256, alpha=1.0),
     synth.small_workload("decode_mixtral", d_model=512, d_ff=1024),
+    synth.small_workload("mixtral_prefill", n_tokens=2048, d_model=256, n_experts=4, d_ff=320, alpha=1.0),
+    synth.small_workload("dsv2", n_tokens=1600, d_model=192, n_experts=4, top_k=2, d_ff=192, n_shared=1),
     synth.small_workload("decode_dsv2", d_model=256, d_ff=256),
 ]
 
