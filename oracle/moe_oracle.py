@@ -30,6 +30,20 @@ the design notes):
      freq_e = picks_e/(N*k), P_e = mean_t p[t,e], L_bal = E * sum_e freq_e*P_e.
   R6 SwiGLU expert: silu(x Wg^T) * (x Wu^T), then Wd; silu(a) = a/(1+e^-a).
   R7 GELU is the erf form, nn.GELU()'s default ([P5] §3 code).
+  R13 router z-loss ([P2] §3.3): L_z = 0.001 * mean_t logsumexp_e(z[t,e])^2 on
+     the router's own logits z = x W_r^T, without the per-expert bias (the
+     bias is not part of the router's linear map).
+  R14 router entropy ([P4] §2.3 and its §3.1 code): per token, the softmax of
+     the k selected logits (= the renormalised gates w), H_t = -sum_j w_j
+     log2 w_j in bits (the page's code uses log2; its 1e-8 guard is left out,
+     0 log 0 = 0), averaged over the tokens.
+  R15 selection-only bias ([P5] §2.4, DeepSeek-V3): the expert bias steers the
+     choice but leaves the router's probabilities alone: p = softmax(z), the
+     top-k is taken on the float32 key p + b (ties to the lower index), the
+     gates renormalise the unbiased p, mean_prob uses p, and reroute ranks
+     candidates by the key.  The per-batch update lowers b_e by gamma when
+     expert e got more than N*k/E pre-capacity picks and raises it by gamma
+     when it got fewer (float32 arithmetic); the pages give no gamma.
 """
 from __future__ import annotations
 
@@ -43,6 +57,7 @@ __all__ = [
     "renormalise", "balance_stats", "alpha_for_batch", "capacity",
     "apply_capacity_drop", "apply_capacity_reroute", "route", "dispatch",
     "gelu_erf", "silu", "expert_ffn", "combine_token", "moe_forward",
+    "router_z_loss", "router_entropy", "selection_keys", "router_bias_update",
 ]
 
 # Parity pins: which CPU test pins each function to something other than itself.
@@ -62,6 +77,14 @@ PINS = {
                               "counts<=C, no duplicate expert, next-best and "
                               "maximality properties",
     "expert_ffn": "tests/test_oracle_ffn.py: erf/exp special values, E=1 dense FFN",
+    "router_z_loss": "tests/test_oracle_next.py: zero logits give 0.001*(ln E)^2, "
+                     "scipy.special.logsumexp, shift by c adds c to lse",
+    "router_entropy": "tests/test_oracle_next.py: equal gates give log2 k, one gate "
+                      "gives 0, hand case (0.75, 0.25) -> 0.8112781 bits",
+    "selection_keys": "tests/test_oracle_next.py: zero bias reduces to the plain "
+                      "router, brute force over subsets of p+b, gates from unbiased p",
+    "router_bias_update": "tests/test_oracle_next.py: hand case of signs, balanced "
+                          "picks leave the bias unchanged",
     "moe_forward": "tests/test_oracle_forward.py: E=1 dense layer, shared-only dense "
                    "layer, token-permutation equivariance, linearity in the gates; "
                    "no page prints a numeric layer output, so beyond these the "
@@ -155,15 +178,76 @@ def balance_stats(p, idx, n_experts):
     return freq, mean_prob, float(n_experts * np.sum(freq * mean_prob))
 
 
-def route(x, w_router, router_bias, k):
-    """Router stage: logits, float32 probabilities, top-k, gates, statistics."""
-    z = router_logits(x, w_router, router_bias)
-    p = softmax_fp32(z)
-    idx = topk_select(p, k)
+def router_z_loss(z):
+    """L_z = 0.001 * mean_t (logsumexp_e z[t,e])^2 -- [P2] §3.3 (reading R13).
+
+    z are the router's logits without the expert bias.  logsumexp is written
+    out as m + log(sum exp(z - m)) with m the row maximum (the same function).
+    """
+    z = np.asarray(z, dtype=np.float64)
+    m = z.max(axis=1)
+    lse = m + np.log(np.exp(z - m[:, None]).sum(axis=1))
+    return 0.001 * float(np.mean(lse * lse)) if len(lse) else 0.0
+
+
+def router_entropy(w):
+    """Mean over tokens of H_t = -sum_j w_j log2 w_j, bits -- [P4] §2.3 (reading R14).
+
+    w are the renormalised top-k gates (the softmax of the selected logits).
+    """
+    w = np.asarray(w, dtype=np.float32).astype(np.float64)
+    if w.shape[0] == 0:
+        return 0.0
+    terms = np.where(w > 0, -w * np.log2(np.where(w > 0, w, 1.0)), 0.0)
+    return float(np.mean(terms.sum(axis=1)))
+
+
+def selection_keys(p, router_bias):
+    """key[t,e] = p[t,e] + b[e] in float32 -- [P5] §2.4 (reading R15)."""
+    return (np.asarray(p, dtype=np.float32) +
+            np.asarray(router_bias, dtype=np.float32)[None, :]).astype(np.float32)
+
+
+def router_bias_update(router_bias, picks, n_tokens, k, gamma):
+    """b_e - gamma if picks_e > N*k/E, b_e + gamma if picks_e < N*k/E -- [P5] §2.4.
+
+    picks are the pre-capacity top-k picks per expert; float32 arithmetic.
+    """
+    b = np.asarray(router_bias, dtype=np.float32).copy()
+    picks = np.asarray(picks, dtype=np.int64)
+    E = len(b)
+    g = np.float32(gamma)
+    for e in range(E):
+        load = picks[e] * E            # compare picks_e with N*k/E without division
+        if load > n_tokens * k:
+            b[e] = np.float32(b[e] - g)
+        elif load < n_tokens * k:
+            b[e] = np.float32(b[e] + g)
+    return b
+
+
+def route(x, w_router, router_bias, k, bias_mode=0):
+    """Router stage: logits, float32 probabilities, top-k, gates, statistics.
+
+    bias_mode 0: the expert bias is added to the logits before the softmax
+    ([P3] §2.2); 1: the bias only steers the selection (reading R15).  "key" is
+    what the top-k and the reroute rank by.
+    """
+    z_raw = router_logits(x, w_router, None)
+    if bias_mode == 1 and router_bias is not None:
+        p = softmax_fp32(z_raw)
+        key = selection_keys(p, router_bias)
+    else:
+        p = softmax_fp32(router_logits(x, w_router, router_bias))
+        key = p
+    idx = topk_select(key, k)
     w = renormalise(p, idx)
     freq, mean_prob, l_bal = balance_stats(p, idx, p.shape[1])
-    return {"logits": z, "p": p, "idx": idx, "w": w, "margin": topk_margin(p, k),
-            "expert_freq": freq, "mean_prob": mean_prob, "l_bal": l_bal}
+    picks = np.bincount(idx.ravel().astype(np.int64), minlength=p.shape[1])
+    return {"logits": z_raw, "p": p, "key": key, "idx": idx, "w": w,
+            "margin": topk_margin(key, k), "expert_freq": freq, "mean_prob": mean_prob,
+            "l_bal": l_bal, "picks": picks, "z_loss": router_z_loss(z_raw),
+            "router_entropy": router_entropy(w)}
 
 
 # ----------------------------------------------------------------------------- capacity
@@ -334,9 +418,10 @@ def moe_forward(cfg, inputs, tokens=None, get_expert=None):
     Returns a dict with routing tensors, statistics and y [len(tokens), d] float64.
     """
     N, E, k, S = cfg.n_tokens, cfg.n_experts, cfg.top_k, cfg.n_shared
-    r = route(inputs["x"], inputs["w_router"], inputs.get("router_bias"), k)
+    r = route(inputs["x"], inputs["w_router"], inputs.get("router_bias"), k,
+              getattr(cfg, "bias_mode", 0))
     cap = capacity(N, E, k, cfg.alpha) if cfg.cap_mode != 0 else None
-    dsp = dispatch(r["idx"], r["p"], E, cfg.cap_mode, cap)
+    dsp = dispatch(r["idx"], r["key"], E, cfg.cap_mode, cap)
     out = dict(r)
     out.update(dsp)
     out["capacity"] = cap

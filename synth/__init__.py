@@ -56,6 +56,7 @@ class Workload:
     has_ffn_bias: bool
     bias_law: str
     seed: int
+    bias_mode: int = 0          # 0: bias added to the logits, 1: selection only
 
     @property
     def has_router_bias(self) -> bool:
@@ -84,6 +85,10 @@ WORKLOADS = {
                                DT_BF16, CAP_NONE, 0.0, False, BIAS_LOGZIPF, 0x4D6F4505),
     "decode_dsv2": Workload("decode_dsv2", 32, 5120, 160, 6, 1536, 2, ACT_SWIGLU, DT_BF16,
                             CAP_NONE, 0.0, False, BIAS_LOGZIPF, 0x4D6F4506),
+    # The DeepSeek-V2-like layer with the bias steering selection only
+    # (DeepSeek-V3 style); same shapes and inputs as "dsv2".
+    "dsv2_select": Workload("dsv2_select", 8192, 5120, 160, 6, 1536, 2, ACT_SWIGLU, DT_BF16,
+                            CAP_NONE, 0.0, False, BIAS_UNIFORM, 0x4D6F4503, bias_mode=1),
 }
 
 # Tensor identifiers inside one workload's seed space.
