@@ -44,6 +44,14 @@ the design notes):
      candidates by the key.  The per-batch update lowers b_e by gamma when
      expert e got more than N*k/E pre-capacity picks and raises it by gamma
      when it got fewer (float32 arithmetic); the pages give no gamma.
+  R16 low-precision expert weights ([P1] §5.4, [P4] §4.4: per-expert scales,
+     the router stays in high precision): FP8 E4M3 (OCP 8-bit floating point
+     format: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, subnormals,
+     no infinities, S.1111.111 is NaN, largest finite 448).  One float32 scale
+     per expert matrix, scale = amax/448 (1 for an all-zero matrix); a code is
+     round-to-nearest-even of the float32 quotient w/scale, saturated to
+     +-448.  Weights only: activations, accumulation and the SwiGLU product
+     stay as in the bf16 layer; the dequantised weight is scale * code value.
 """
 from __future__ import annotations
 
@@ -58,6 +66,7 @@ __all__ = [
     "apply_capacity_drop", "apply_capacity_reroute", "route", "dispatch",
     "gelu_erf", "silu", "expert_ffn", "combine_token", "moe_forward",
     "router_z_loss", "router_entropy", "selection_keys", "router_bias_update",
+    "e4m3_encode", "e4m3_decode", "quantize_fp8", "dequantize_fp8",
 ]
 
 # Parity pins: which CPU test pins each function to something other than itself.
@@ -85,6 +94,13 @@ PINS = {
                       "router, brute force over subsets of p+b, gates from unbiased p",
     "router_bias_update": "tests/test_oracle_next.py: hand case of signs, balanced "
                           "picks leave the bias unchanged",
+    "e4m3_encode": "tests/test_oracle_fp8.py: torch float8_e4m3fn cast (library) on "
+                   "random, tie and subnormal values; saturation and signed zero by hand",
+    "e4m3_decode": "tests/test_oracle_fp8.py: all 256 codes vs torch float8_e4m3fn, "
+                   "encode(decode(c)) == c for every finite code",
+    "quantize_fp8": "tests/test_oracle_fp8.py: largest element maps to 448, error "
+                    "<= half a step, zero matrix, hand case",
+    "dequantize_fp8": "tests/test_oracle_fp8.py: product of the decoded code and the scale",
     "moe_forward": "tests/test_oracle_forward.py: E=1 dense layer, shared-only dense "
                    "layer, token-permutation equivariance, linearity in the gates; "
                    "no page prints a numeric layer output, so beyond these the "
@@ -142,16 +158,18 @@ def topk_select(p, k):
 
 
 def topk_margin(p, k):
-    """p_(k) - p_(k+1) per token on the float32 probabilities (inf when k == E).
+    """Smallest gap between consecutive float32 scores among the k+1 largest
+    (among all E when k == E), per token.
 
-    Used to flag near-ties: tokens whose margin is below 1e-6 may legitimately
-    select differently on hardware that rounds the logits differently."""
+    Used to flag near-ties: a token whose gap is below 1e-6 may legitimately
+    select a different set, or order its selected experts differently, on
+    hardware that rounds the scores differently."""
     p = np.asarray(p, dtype=np.float32).astype(np.float64)
     E = p.shape[1]
-    if k >= E:
+    s = -np.sort(-p, axis=1)[:, :min(k + 1, E)]
+    if s.shape[1] < 2:
         return np.full(p.shape[0], np.inf)
-    s = -np.sort(-p, axis=1)
-    return s[:, k - 1] - s[:, k]
+    return np.min(s[:, :-1] - s[:, 1:], axis=1)
 
 
 def renormalise(p, idx):
@@ -248,6 +266,66 @@ def route(x, w_router, router_bias, k, bias_mode=0):
             "margin": topk_margin(key, k), "expert_freq": freq, "mean_prob": mean_prob,
             "l_bal": l_bal, "picks": picks, "z_loss": router_z_loss(z_raw),
             "router_entropy": router_entropy(w)}
+
+
+# ----------------------------------------------------------------------------- fp8 weights
+
+E4M3_MAX = 448.0
+
+
+def e4m3_encode(v):
+    """float32 values -> FP8 E4M3 codes (uint8), round to nearest even, saturated.
+
+    Reading R16.  Normal numbers are (1 + m/8) * 2^(e-7) for exponent field
+    e = 1..15 and mantissa m = 0..7 (e = 15, m = 7 is NaN); subnormals are
+    m * 2^-9.  A magnitude at or above 448 saturates to 448.
+    """
+    v = np.asarray(v, dtype=np.float32).astype(np.float64)
+    sign = np.signbit(v).astype(np.uint8) << 7
+    a = np.abs(v)
+    code = np.zeros(a.shape, dtype=np.int64)
+    sub = a < 2.0 ** -6
+    # subnormal range: multiples of 2^-9 (a result of 8 is the smallest normal, code 8)
+    code[sub] = np.rint(a[sub] / 2.0 ** -9).astype(np.int64)
+    nrm = ~sub & (a < E4M3_MAX)
+    if np.any(nrm):
+        _, ex = np.frexp(a[nrm])             # a = f * 2^ex, f in [0.5, 1)
+        e = ex - 1                           # a in [2^e, 2^(e+1))
+        m = np.rint(a[nrm] / 2.0 ** (e - 3)).astype(np.int64)   # 8 .. 16
+        carry = m == 16
+        e = np.where(carry, e + 1, e)
+        m = np.where(carry, 8, m)
+        code[nrm] = ((e + 7) << 3) | (m - 8)
+    code[a >= E4M3_MAX] = 0x7E
+    return (code.astype(np.uint8) | sign).astype(np.uint8)
+
+
+def e4m3_decode(code):
+    """FP8 E4M3 codes -> float64 values (NaN for S.1111.111)."""
+    c = np.asarray(code, dtype=np.uint8).astype(np.int64)
+    s = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 15
+    m = c & 7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
+    return s * mag
+
+
+def quantize_fp8(w):
+    """One expert matrix (bf16 bit patterns or float32) -> (codes uint8, scale float32).
+
+    scale = amax/448 in float32 (1 when the matrix is all zero); code =
+    e4m3_encode(float32(w) / scale) with a float32 division (reading R16).
+    """
+    wf = widen(w).astype(np.float32)
+    amax = np.float32(np.max(np.abs(wf))) if wf.size else np.float32(0)
+    scale = np.float32(amax / np.float32(E4M3_MAX)) if amax > 0 else np.float32(1.0)
+    return e4m3_encode((wf / scale).astype(np.float32)), scale
+
+
+def dequantize_fp8(codes, scale):
+    """scale * value(code), float64 (exact)."""
+    return e4m3_decode(codes) * float(np.float32(scale))
 
 
 # ----------------------------------------------------------------------------- capacity

@@ -68,7 +68,9 @@ def test_k_equals_E_every_expert_fires_and_gates_equal_p():
     assert all(sorted(r) == list(range(E)) for r in idx.tolist())
     w = oracle.renormalise(p, idx)
     np.testing.assert_allclose(w, np.take_along_axis(p, idx.astype(np.int64), 1), rtol=2e-7)
-    assert np.all(np.isinf(oracle.topk_margin(p, E)))
+    # with k == E only the slot order can flip: the margin is the smallest gap
+    srt = -np.sort(-p.astype(np.float64), axis=1)
+    np.testing.assert_array_equal(oracle.topk_margin(p, E), np.min(srt[:, :-1] - srt[:, 1:], axis=1))
 
 
 def test_zero_router_gives_uniform_probabilities():
@@ -102,3 +104,8 @@ def test_margin_flags_near_ties():
     p = np.array([[0.5, 0.25, 0.25 - 2 ** -25, 0.0]], dtype=np.float32)
     m = oracle.topk_margin(p, 2)
     assert 0 < m[0] < 1e-6
+    # a near-tie inside the selected set (slot order) is flagged too
+    q = np.array([[0.4, 0.4 - 2 ** -24, 0.1, 0.1 - 0.05]], dtype=np.float32)
+    assert 0 < oracle.topk_margin(q, 2)[0] < 1e-6
+    assert oracle.topk_margin(np.array([[0.5, 0.3, 0.2, 0.0]], np.float32), 2)[0] == \
+        np.float64(np.float32(0.3)) - np.float64(np.float32(0.2))
