@@ -182,6 +182,20 @@ def layer_work(w, counts_kept, n_dropped):
             "total_flop": g1 + g2 + router}
 
 
+def gemm1_kernel(w) -> str:
+    """The gate/up GEMM kernel the library launches for this workload: the
+    weights-as-M (swap-AB) kernel for E4M3 weights and for batches with at most
+    64 assignments per expert on average (and, with shared experts, at most 512
+    tokens); the 128-row-tile kernel otherwise (the rule in csrc/ffn_tc.cu)."""
+    if w.dtype != synth.DT_BF16:
+        return "ffn_simt_kernel<1>"
+    if w.fp8_weights:
+        return "ffn_tc_swap_kernel<0,fp8>"
+    if w.n_tokens * w.top_k <= 64 * w.n_experts and (w.n_shared == 0 or w.n_tokens <= 512):
+        return "ffn_tc_swap_kernel<0>"
+    return "ffn_tc_kernel<0>"
+
+
 def measured_traffic(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` on `workload` from a committed ncu capture
     (profiles/ncu_traffic.json), or None when there is none or the kernel's source
@@ -235,9 +249,26 @@ def to_dev(a, device):
     return torch.from_numpy(np.ascontiguousarray(a)).to(device)
 
 
+def oracle_experts(w, inp):
+    """The oracle's expert weights: None (take them from `inp`), or for E4M3
+    workloads a getter that quantises and dequantises an expert on each call."""
+    if not w.fp8_weights:
+        return None
+    import oracle
+
+    def get(e):
+        out = {"b1": None, "b2": None}
+        for key in ("w_gate", "w_up", "w_down"):
+            codes, scale = oracle.quantize_fp8(inp[key][e])
+            out[key] = oracle.dequantize_fp8(codes, scale)
+        return out
+    return get
+
+
 def run_cpu_oracle(w, inp, budget_s=20.0, max_tokens=None):
     """Time the oracle (as it stands) on a bounded token sample; returns tokens/s."""
     import oracle
+    get = oracle_experts(w, inp)
     try:
         from threadpoolctl import threadpool_info
         cores = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
@@ -247,7 +278,7 @@ def run_cpu_oracle(w, inp, budget_s=20.0, max_tokens=None):
     n, dt = 1, 0.0
     while True:
         t0 = time.perf_counter()
-        oracle.moe_forward(w, inp, tokens=np.arange(n))
+        oracle.moe_forward(w, inp, tokens=np.arange(n), get_expert=get)
         dt = time.perf_counter() - t0
         if dt >= budget_s / 3 or n >= w.n_tokens or (max_tokens and n >= max_tokens):
             break
@@ -269,9 +300,10 @@ def bench_reference(args, w):
     info = run_cpu_oracle(w, inp, budget_s=3 * budget, max_tokens=args.ref_tokens)
     n = int(info["sample"].split("first ")[1].split(" ")[0])
     per_step = []
+    get = oracle_experts(w, inp)
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        oracle.moe_forward(w, inp, tokens=np.arange(n))
+        oracle.moe_forward(w, inp, tokens=np.arange(n), get_expert=get)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             per_step.append(dt)
@@ -297,6 +329,9 @@ def workload_config(w, world):
             "activation": "swiglu" if w.act == synth.ACT_SWIGLU else "gelu",
             "capacity": ["none", "drop", "reroute"][w.cap_mode],
             "alpha": w.alpha if w.cap_mode else None, "router_bias": w.bias_law,
+            "router_bias_mode": "selection" if w.bias_mode else "logit",
+            "expert_weights": "fp8_e4m3" if w.fp8_weights else
+            ("bf16" if w.dtype == synth.DT_BF16 else "f32"),
             "l2_flush": True, "parallelism": f"replicas{world}" if world > 1 else "single"}
 
 
@@ -311,7 +346,8 @@ def bench_ours(args, w):
     torch.cuda.set_device(dev)
     cfg = moe.make_config(w.n_tokens, w.d_model, w.n_experts, w.top_k, w.d_ff, w.n_shared,
                           act=w.act, dtype=w.dtype, cap_mode=w.cap_mode, alpha=w.alpha,
-                          has_ffn_bias=w.has_ffn_bias, has_router_bias=w.has_router_bias)
+                          has_ffn_bias=w.has_ffn_bias, has_router_bias=w.has_router_bias,
+                          bias_mode=w.bias_mode)
     inp = synth.make_inputs(w)
     x = to_dev(inp["x"], dev)
     wr = to_dev(inp["w_router"], dev)
@@ -325,15 +361,34 @@ def bench_ours(args, w):
             "l_bal": torch.zeros(1, device=dev),
             "counts": torch.zeros(E, dtype=torch.int32, device=dev),
             "n_dropped": torch.zeros(1, dtype=torch.int32, device=dev),
-            "n_rerouted": torch.zeros(1, dtype=torch.int32, device=dev)}
+            "n_rerouted": torch.zeros(1, dtype=torch.int32, device=dev),
+            "z_loss": torch.zeros(1, device=dev), "router_entropy": torch.zeros(1, device=dev)}
     stats = moe.make_stats(**st_t)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    args_f = (cfg, x, wr, rb, wg, wu, wd, b1, b2, y)
+    if w.fp8_weights:
+        # E4M3 codes and per-expert-matrix scales, made by the library before timing
+        qw, sc = [], []
+        for t in (wg, wu, wd):
+            q = torch.empty(t.shape, dtype=torch.uint8, device=dev)
+            s_ = torch.empty(t.shape[0], dtype=torch.float32, device=dev)
+            moe.moe_quantize_fp8(t, q, s_, stream)
+            qw.append(q)
+            sc.append(s_)
+        scales = torch.stack(sc).contiguous()
+        del wg, wu, wd
+        torch.cuda.synchronize()
+
+    def forward(x_arg, timing=None):
+        if w.fp8_weights:
+            return moe.moe_forward_fp8(cfg, x_arg, wr, rb, qw[0], qw[1], qw[2], scales, y, stats,
+                                       ws, stream, timing=timing)
+        return moe.moe_forward(cfg, x_arg, wr, rb, wg, wu, wd, b1, b2, y, stats, ws, stream,
+                               timing=timing)
 
     # warm-up
     for _ in range(args.warmup):
-        moe.moe_forward(*args_f, stats, ws, stream)
+        forward(x)
     torch.cuda.synchronize()
     if moe.moe_device_status(ws) != moe.MOE_OK:
         raise RuntimeError("device status not ok after warm-up")
@@ -360,7 +415,7 @@ def bench_ours(args, w):
     with ClockSampler(dev) as clk:
         for s in range(args.steps):
             flush.fill_(s & 0xFF)
-            moe.moe_forward(*args_f, stats, ws, stream, timing=timings[s])
+            forward(x, timings[s])
         torch.cuda.synchronize()
     launches = moe.moe_kernel_launches() - launches0
     if world > 1:
@@ -386,7 +441,7 @@ def bench_ours(args, w):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         x_in.view(x_host.dtype).copy_(x_host, non_blocking=True)
-        moe.moe_forward(cfg, x_in, wr, rb, wg, wu, wd, b1, b2, y, stats, ws, stream)
+        forward(x_in)
         y_host.copy_(y.view(y_host.dtype), non_blocking=True)
         e1.record(stream)
         e1.synchronize()
@@ -397,13 +452,14 @@ def bench_ours(args, w):
     pk = peaks()
     counts = st_t["counts"].cpu().numpy()
     es = 2 if w.dtype == synth.DT_BF16 else 4
+    wes = 1 if w.fp8_weights else es             # bytes per expert-weight element
     touched = int((counts > 0).sum()) + w.n_shared
     nmat1 = 2 if w.act == synth.ACT_SWIGLU else 1
     rows = work["rows"]
     # algorithmic bytes of the first expert GEMM: weights of touched experts, its
     # input rows, its output rows
-    g1_wbytes = touched * nmat1 * w.d_ff * w.d_model * es
-    g2_wbytes = touched * w.d_ff * w.d_model * es
+    g1_wbytes = touched * nmat1 * w.d_ff * w.d_model * wes
+    g2_wbytes = touched * w.d_ff * w.d_model * wes
     g1_bytes = g1_wbytes + rows * w.d_model * es + rows * w.d_ff * es
     g1_ms = statistics.mean(stage["gemm1"])
     g1_tflops = work["gemm1_flop"] / (g1_ms * 1e-3) / 1e12
@@ -420,8 +476,9 @@ def bench_ours(args, w):
         roof = {"bound": "hbm", "achieved": g1_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": frac_b, "peak_source": f"{pk['source']} copy bandwidth",
                 "algorithmic_per_launch": g1_bytes}
-    roof.update({"kernel": "ffn_tc_kernel<0> (gate/up GEMM + SwiGLU)",
-                 "traffic": measured_traffic("ffn_tc_kernel<0>", w.name),
+    kname = gemm1_kernel(w)
+    roof.update({"kernel": kname + " (gate/up GEMM + SwiGLU)",
+                 "traffic": measured_traffic(kname, w.name),
                  "algorithmic_bytes_per_launch": g1_bytes})
     step_s = total_ms / args.steps * 1e-3
     value = throughput(w.n_tokens, args.steps, world, total_ms)
@@ -442,6 +499,8 @@ def bench_ours(args, w):
         "layer_weight_gbs": (g1_wbytes + g2_wbytes) / step_s / 1e9,
         "layer_weight_frac_hbm": (g1_wbytes + g2_wbytes) / step_s / 1e9 / pk["hbm_gbs"],
         "experts_touched": touched, "kept_assignments": kept, "dropped": nd,
+        "router_stats": {"l_bal": float(st_t["l_bal"][0]), "z_loss": float(st_t["z_loss"][0]),
+                         "router_entropy_bits": float(st_t["router_entropy"][0])},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = run_cpu_oracle(w, inp, budget_s=args.ref_budget or 15.0,

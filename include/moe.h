@@ -71,6 +71,12 @@ typedef enum {
 typedef enum { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1 } moe_act;
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 typedef enum { MOE_CAP_NONE = 0, MOE_CAP_DROP = 1, MOE_CAP_REROUTE = 2 } moe_cap_mode;
+/* How router_bias enters the routing.  LOGIT: added to the logits before the
+ * softmax («DeepSeek-V2 ...» summary §2.2 TopKRouter).  SELECT: the softmax is
+ * of the bias-free logits and the bias only steers the choice, top-k of
+ * p + b with gates renormalised from p («为什么MoE有效？...» §2.4, the
+ * DeepSeek-V3 auxiliary-loss-free scheme). */
+typedef enum { MOE_BIAS_LOGIT = 0, MOE_BIAS_SELECT = 1 } moe_bias_mode;
 
 #define MOE_MAX_EXPERTS 256      /* routed experts E                      */
 #define MOE_MAX_TOPK 8           /* k <= min(E, 8)                        */
@@ -91,7 +97,8 @@ typedef struct moe_config {
   int32_t cap_mode;        /* moe_cap_mode                                 */
   float alpha;             /* capacity factor (> 0 unless MOE_CAP_NONE)    */
   int32_t has_ffn_bias;    /* GELU experts: b1 [E+S, F], b2 [E+S, d]       */
-  int32_t has_router_bias; /* router_bias [E] fp32 is added to the logits  */
+  int32_t has_router_bias; /* router_bias [E] fp32 is given                */
+  int32_t bias_mode;       /* moe_bias_mode (with has_router_bias)         */
 } moe_config;
 
 /* Statistics outputs (device pointers; each may be NULL = not written). */
@@ -102,6 +109,10 @@ typedef struct moe_stats {
   int32_t* counts;     /* [E]  assignments kept per routed expert (post-cap)  */
   int32_t* n_dropped;  /* [1]  assignments dropped by capacity                */
   int32_t* n_rerouted; /* [1]  assignments moved to another expert            */
+  float* z_loss;       /* [1]  0.001 * mean_t logsumexp(z_t)^2 on the bias-free
+                                logits («项目概述：为什么MoE...» §3.3)           */
+  float* router_entropy; /* [1] mean_t -sum_j w_tj log2 w_tj over the gates, bits
+                                («GPT-4 Has 1.8 Trillion Parameters...» §2.3)  */
 } moe_stats;
 
 /* Optional stage timing for moe_forward: cudaEvent_t handles (as void*),
@@ -159,13 +170,18 @@ int64_t moe_kernel_launches(void);
 /* ---- device calls ---------------------------------------------------------- */
 
 /* Router: logits, fp32 softmax, top-k with renormalised gates, and the
- * pre-capacity statistics (expert_freq, mean_prob, l_bal).
+ * pre-capacity statistics (expert_freq, mean_prob, l_bal, z_loss,
+ * router_entropy).
  *   x        [N, d]      w_router [E, d]      router_bias [E] fp32 (NULL unless
  *   has_router_bias)
- *   topk_idx [N, k] int32 out, slot 0 = most probable expert
+ *   topk_idx [N, k] int32 out, slot 0 = highest selection score
  *   topk_w   [N, k] fp32  out, renormalised gates (sum 1 per token)
- *   probs    [N, E] fp32  out, nullable
- *   stats    nullable; expert_freq, mean_prob, l_bal are written if non-NULL. */
+ *   probs    [N, E] fp32  out, nullable: the selection scores the top-k ranks
+ *            (the probabilities; p + b under MOE_BIAS_SELECT), which is what
+ *            moe_dispatch's reroute ranks by
+ *   stats    nullable; expert_freq, mean_prob, l_bal, z_loss, router_entropy
+ *            are written where non-NULL (mean_prob averages the probabilities,
+ *            never p + b). */
 int moe_route(const moe_config* cfg, const void* x, const void* w_router,
               const float* router_bias, int32_t* topk_idx, float* topk_w, float* probs,
               const moe_stats* stats, void* workspace, size_t workspace_bytes, void* stream);
@@ -173,8 +189,8 @@ int moe_route(const moe_config* cfg, const void* x, const void* w_router,
 /* Dispatch: per-expert histogram, scan, capacity (drop or reroute), segment
  * layout and the permutation of token rows into x_perm.
  *   topk_idx  [N, k] int32 in (as written by moe_route)
- *   probs     [N, E] fp32 in, required when cap_mode == REROUTE (candidate
- *             order), else may be NULL
+ *   probs     [N, E] fp32 in, required when cap_mode == REROUTE: the
+ *             selection scores moe_route wrote (candidate order), else may be NULL
  *   x         [N, d] in
  *   final_idx [N, k] int32 out: expert of the slot after capacity, -1 dropped
  *   pos       [N, k] int32 out: row of the slot in the expert-row space, -1 dropped
@@ -225,6 +241,51 @@ int moe_forward(const moe_config* cfg, const void* x, const void* w_router,
                 const void* w_down, const void* b1, const void* b2, void* y,
                 const moe_stats* stats, void* workspace, size_t workspace_bytes,
                 void* stream, const moe_timing* timing);
+
+/* Auxiliary-loss-free balancing step («为什么MoE有效？...» §2.4): for each
+ * expert e, router_bias[e] -= gamma if e got more than N*k/E pre-capacity
+ * picks in the last moe_route / moe_forward run on `workspace`, += gamma if
+ * fewer, unchanged if equal (fp32 arithmetic).  router_bias [E] fp32 device,
+ * updated in place on `stream`, ordered after that run.  The pages give no
+ * gamma. */
+int moe_router_bias_update(const moe_config* cfg, const void* workspace, size_t workspace_bytes,
+                           float* router_bias, float gamma, void* stream);
+
+/* ---- FP8 (E4M3) expert weights --------------------------------------------
+ * «大模型MoE架构揭秘：如何用2%参数实现万亿级算力调度» §5.4 and «GPT-4 Has 1.8
+ * Trillion Parameters...» §4.4: expert weights in low precision with
+ * per-expert scales, router kept in high precision.  Format: OCP FP8 E4M3
+ * (bias 7, 3 mantissa bits, subnormals, largest finite 448, no infinities).
+ * Weights only: activations stay bf16, accumulation fp32, H is bf16 as in the
+ * bf16 layer.  The dequantised weight is scale * value(code). */
+
+/* Quantise n_mat bf16 matrices of rows x cols each (contiguous, row-major):
+ * per matrix scale = amax / 448 in fp32 (1 if the matrix is all zero), code =
+ * round-to-nearest-even of the fp32 quotient w / scale, saturated to +-448.
+ *   w      [n_mat, rows, cols] bf16 in     q [n_mat, rows, cols] uint8 out
+ *   scales [n_mat] fp32 out
+ * rows * cols must be a multiple of 16; 1 <= n_mat <= 65535. */
+int moe_quantize_fp8(const void* w, int32_t n_mat, int64_t rows, int64_t cols, uint8_t* q,
+                     float* scales, void* stream);
+
+/* moe_expert_ffn with E4M3 weights (dtype MOE_BF16, MOE_ACT_SWIGLU, no FFN
+ * bias; d_model and d_ff multiples of 16).
+ *   w_gate, w_up [E+S, F, d] and w_down [E+S, d, F] E4M3 codes
+ *   scales [3, E+S] fp32: gate, up and down scale of each expert
+ *   counts [E] required (kept rows per routed expert)
+ * Other arguments as moe_expert_ffn. */
+int moe_expert_ffn_fp8(const moe_config* cfg, const void* x, const void* x_perm,
+                       const int32_t* offsets, const int32_t* counts, const uint8_t* w_gate,
+                       const uint8_t* w_up, const uint8_t* w_down, const float* scales,
+                       void* y_perm, void* workspace, size_t workspace_bytes, void* stream);
+
+/* moe_forward with E4M3 expert weights (same conditions as
+ * moe_expert_ffn_fp8); the router runs on the bf16 w_router as in moe_forward. */
+int moe_forward_fp8(const moe_config* cfg, const void* x, const void* w_router,
+                    const float* router_bias, const uint8_t* w_gate, const uint8_t* w_up,
+                    const uint8_t* w_down, const float* scales, void* y, const moe_stats* stats,
+                    void* workspace, size_t workspace_bytes, void* stream,
+                    const moe_timing* timing);
 
 /* Dispatch without a workspace.  No page has a counterpart: it exists for
  * callers that cannot allocate device memory when they run the layer (a

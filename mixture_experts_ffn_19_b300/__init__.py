@@ -26,6 +26,7 @@ MOE_ERR_DEVICE = -6
 MOE_ACT_GELU, MOE_ACT_SWIGLU = 0, 1
 MOE_F32, MOE_BF16 = 0, 1
 MOE_CAP_NONE, MOE_CAP_DROP, MOE_CAP_REROUTE = 0, 1, 2
+MOE_BIAS_LOGIT, MOE_BIAS_SELECT = 0, 1
 MOE_SEGMENT_ALIGN = 128
 
 
@@ -41,13 +42,15 @@ class moe_config(ctypes.Structure):
                 ("d_ff", ctypes.c_int32), ("n_shared", ctypes.c_int32),
                 ("act", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("cap_mode", ctypes.c_int32), ("alpha", ctypes.c_float),
-                ("has_ffn_bias", ctypes.c_int32), ("has_router_bias", ctypes.c_int32)]
+                ("has_ffn_bias", ctypes.c_int32), ("has_router_bias", ctypes.c_int32),
+                ("bias_mode", ctypes.c_int32)]
 
 
 class moe_stats(ctypes.Structure):
     _fields_ = [("expert_freq", ctypes.c_void_p), ("mean_prob", ctypes.c_void_p),
                 ("l_bal", ctypes.c_void_p), ("counts", ctypes.c_void_p),
-                ("n_dropped", ctypes.c_void_p), ("n_rerouted", ctypes.c_void_p)]
+                ("n_dropped", ctypes.c_void_p), ("n_rerouted", ctypes.c_void_p),
+                ("z_loss", ctypes.c_void_p), ("router_entropy", ctypes.c_void_p)]
 
 
 class moe_timing(ctypes.Structure):
@@ -81,6 +84,14 @@ _SIGS = {
     "moe_forward": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    ctypes.POINTER(moe_stats), _P, ctypes.c_size_t, _P,
                                    ctypes.POINTER(moe_timing)]),
+    "moe_router_bias_update": (ctypes.c_int, [_CFG, _P, ctypes.c_size_t, _P, ctypes.c_float, _P]),
+    "moe_quantize_fp8": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, _P, _P,
+                                        _P]),
+    "moe_expert_ffn_fp8": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                          ctypes.c_size_t, _P]),
+    "moe_forward_fp8": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P,
+                                       ctypes.POINTER(moe_stats), _P, ctypes.c_size_t, _P,
+                                       ctypes.POINTER(moe_timing)]),
     "moe_device_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "moe_kernel_launches": (ctypes.c_int64, []),
 }
@@ -131,16 +142,16 @@ def _check(name: str, st: int) -> int:
 
 def make_config(n_tokens, d_model, n_experts, top_k, d_ff, n_shared=0, act=MOE_ACT_SWIGLU,
                 dtype=MOE_BF16, cap_mode=MOE_CAP_NONE, alpha=0.0, has_ffn_bias=False,
-                has_router_bias=False) -> moe_config:
+                has_router_bias=False, bias_mode=MOE_BIAS_LOGIT) -> moe_config:
     return moe_config(int(n_tokens), int(d_model), int(n_experts), int(top_k), int(d_ff),
                       int(n_shared), int(act), int(dtype), int(cap_mode), float(alpha),
-                      int(bool(has_ffn_bias)), int(bool(has_router_bias)))
+                      int(bool(has_ffn_bias)), int(bool(has_router_bias)), int(bias_mode))
 
 
 def make_stats(expert_freq=None, mean_prob=None, l_bal=None, counts=None, n_dropped=None,
-               n_rerouted=None) -> moe_stats:
+               n_rerouted=None, z_loss=None, router_entropy=None) -> moe_stats:
     return moe_stats(_ptr(expert_freq), _ptr(mean_prob), _ptr(l_bal), _ptr(counts),
-                     _ptr(n_dropped), _ptr(n_rerouted))
+                     _ptr(n_dropped), _ptr(n_rerouted), _ptr(z_loss), _ptr(router_entropy))
 
 
 def moe_validate_config(cfg: moe_config) -> int:
@@ -207,6 +218,37 @@ def moe_forward(cfg, x, w_router, router_bias, w_gate, w_up, w_down, b1, b2, y, 
     return _check("moe_forward", lib().moe_forward(
         ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(w_gate), _ptr(w_up),
         _ptr(w_down), _ptr(b1), _ptr(b2), _ptr(y),
+        ctypes.byref(stats) if stats is not None else None,
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream),
+        ctypes.byref(timing) if timing is not None else None))
+
+
+def moe_router_bias_update(cfg, workspace, router_bias, gamma, stream=None) -> int:
+    return _check("moe_router_bias_update", lib().moe_router_bias_update(
+        ctypes.byref(cfg), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(router_bias), float(gamma), _stream(stream)))
+
+
+def moe_quantize_fp8(w, q, scales, stream=None) -> int:
+    """w [n_mat, rows, cols] bf16 -> q (uint8, same shape), scales [n_mat] fp32."""
+    n_mat, rows, cols = w.shape
+    return _check("moe_quantize_fp8", lib().moe_quantize_fp8(
+        _ptr(w), int(n_mat), int(rows), int(cols), _ptr(q), _ptr(scales), _stream(stream)))
+
+
+def moe_expert_ffn_fp8(cfg, x, x_perm, offsets, counts, w_gate, w_up, w_down, scales, y_perm,
+                       workspace=None, stream=None) -> int:
+    return _check("moe_expert_ffn_fp8", lib().moe_expert_ffn_fp8(
+        ctypes.byref(cfg), _ptr(x), _ptr(x_perm), _ptr(offsets), _ptr(counts), _ptr(w_gate),
+        _ptr(w_up), _ptr(w_down), _ptr(scales), _ptr(y_perm), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_forward_fp8(cfg, x, w_router, router_bias, w_gate, w_up, w_down, scales, y, stats=None,
+                    workspace=None, stream=None, timing=None) -> int:
+    return _check("moe_forward_fp8", lib().moe_forward_fp8(
+        ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(w_gate), _ptr(w_up),
+        _ptr(w_down), _ptr(scales), _ptr(y),
         ctypes.byref(stats) if stats is not None else None,
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream),
         ctypes.byref(timing) if timing is not None else None))

@@ -22,7 +22,7 @@ int64_t align_rows(int64_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Layout {
-  size_t status, acc_p, acc_pick, ticket, zero_end;  // [status .. zero_end) is cleared per call
+  size_t status, acc_p, acc_pick, ticket, acc_zh, zero_end;  // [status .. zero_end) is cleared per call
   size_t topk_idx, topk_w, probs, final_idx, slot, pos, offsets, counts, perm;
   size_t part, chunk_cnt, local_rank, rr_state, rr_scratch;
   size_t x_perm, h, y_perm, total;
@@ -47,6 +47,7 @@ Layout layout_of(const moe_config* c) {
   L.acc_p = take(E * 8);
   L.acc_pick = take(E * 4);
   L.ticket = take(4);
+  L.acc_zh = take(2 * 8);
   L.zero_end = off;
   L.topk_idx = take(N * k * 4);
   L.topk_w = take(N * k * 4);
@@ -102,13 +103,18 @@ int route_impl(const moe_config* c, const void* x, const void* w_router, const f
   const Layout L = layout_of(c);
   RouteParams rp{};
   rp.x = x; rp.w_router = w_router; rp.bias = c->has_router_bias ? bias : nullptr;
+  rp.bias_select = c->bias_mode == MOE_BIAS_SELECT;
   rp.N = c->n_tokens; rp.d = c->d_model; rp.E = c->n_experts; rp.k = c->top_k;
   rp.topk_idx = topk_idx; rp.topk_w = topk_w; rp.probs = probs;
   rp.part = at<float>(ws, L.part);
   rp.acc_p = at<unsigned long long>(ws, L.acc_p);
   rp.acc_pick = at<int>(ws, L.acc_pick);
   rp.ticket = at<unsigned>(ws, L.ticket);
-  if (stats) { rp.expert_freq = stats->expert_freq; rp.mean_prob = stats->mean_prob; rp.l_bal = stats->l_bal; }
+  rp.acc_zh = at<unsigned long long>(ws, L.acc_zh);
+  if (stats) {
+    rp.expert_freq = stats->expert_freq; rp.mean_prob = stats->mean_prob; rp.l_bal = stats->l_bal;
+    rp.z_loss = stats->z_loss; rp.entropy = stats->router_entropy;
+  }
   rp.status = at<int>(ws, L.status);
   return launch_route(rp, c->dtype == MOE_BF16, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -139,8 +145,8 @@ int dispatch_impl(const moe_config* c, const int32_t* topk_idx, const float* pro
 
 int ffn_impl(const moe_config* c, const void* x, const void* x_perm, const int32_t* offsets,
              const int32_t* counts, const void* w_gate, const void* w_up, const void* w_down,
-             const void* b1, const void* b2, void* y_perm, void* ws, cudaStream_t s,
-             cudaEvent_t mid) {
+             const void* b1, const void* b2, const float* w_scales, void* y_perm, void* ws,
+             cudaStream_t s, cudaEvent_t mid) {
   const Layout L = layout_of(c);
   FfnParams fp{};
   fp.N = c->n_tokens; fp.d = c->d_model; fp.F = c->d_ff; fp.E = c->n_experts;
@@ -152,6 +158,7 @@ int ffn_impl(const moe_config* c, const void* x, const void* x_perm, const int32
   fp.max_rows = max_rows_of(c); fp.max_total_rows = max_total_rows_of(c);
   fp.status = at<int>(ws, L.status);
   fp.num_sms = num_sms();
+  fp.w_scales = w_scales;
   const cudaError_t err = c->dtype == MOE_BF16 ? launch_ffn_tc(fp, s, mid) : launch_ffn_simt(fp, s, mid);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -162,6 +169,63 @@ int combine_impl(const moe_config* c, const void* y_perm, const int32_t* offsets
   CombineParams cp{c->n_tokens, c->d_model, c->n_experts, c->top_k, c->n_shared,
                    y_perm, offsets, final_idx, pos, topk_w, y};
   return launch_combine(cp, c->dtype == MOE_BF16, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// The layer, after the caller-specific weight checks: the bf16/fp32 weights
+// (w_scales null) or E4M3 codes with their scales.
+int forward_impl(const moe_config* c, const void* x, const void* w_router, const float* bias,
+                 const void* w_gate, const void* w_up, const void* w_down, const void* b1,
+                 const void* b2, const float* w_scales, void* y, const moe_stats* stats, void* ws,
+                 size_t ws_bytes, void* stream, const moe_timing* timing) {
+  int st = check_ws(c, ws, ws_bytes);
+  if (st != MOE_OK) return st;
+  if (!x || !w_router || !w_gate || !w_down || !y) return MOE_ERR_INVALID_ARG;
+  if (c->has_router_bias && !bias) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(w_gate) || !aligned16(w_down) ||
+      !aligned16(y) || (w_up && !aligned16(w_up)))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Layout L = layout_of(c);
+  if (cudaMemsetAsync(ws, 0, L.zero_end, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (c->n_tokens == 0) return MOE_OK;
+  float* probs = c->cap_mode == MOE_CAP_REROUTE ? at<float>(ws, L.probs) : nullptr;
+  record(timing, 0, s);
+  st = route_impl(c, x, w_router, bias, at<int32_t>(ws, L.topk_idx), at<float>(ws, L.topk_w),
+                  probs, stats, ws, s);
+  if (st != MOE_OK) return st;
+  record(timing, 1, s);
+  // the expert GEMMs read the per-expert counts: the caller's array when given
+  moe_stats st_fwd{};
+  if (stats) st_fwd = *stats;
+  if (!st_fwd.counts) st_fwd.counts = at<int32_t>(ws, L.counts);
+  st = dispatch_impl(c, at<int32_t>(ws, L.topk_idx), probs, x, at<int32_t>(ws, L.final_idx),
+                     at<int32_t>(ws, L.pos), at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.perm),
+                     at<void>(ws, L.x_perm), &st_fwd, ws, s);
+  if (st != MOE_OK) return st;
+  record(timing, 2, s);
+  st = ffn_impl(c, x, at<void>(ws, L.x_perm), at<int32_t>(ws, L.offsets), st_fwd.counts, w_gate,
+                w_up, w_down, b1, b2, w_scales, at<void>(ws, L.y_perm), ws, s,
+                timing ? static_cast<cudaEvent_t>(timing->events[3]) : nullptr);
+  if (st != MOE_OK) return st;
+  record(timing, 4, s);
+  st = combine_impl(c, at<void>(ws, L.y_perm), at<int32_t>(ws, L.offsets),
+                    at<int32_t>(ws, L.final_idx), at<int32_t>(ws, L.pos), at<float>(ws, L.topk_w),
+                    y, s);
+  if (st != MOE_OK) return st;
+  record(timing, 5, s);
+  return MOE_OK;
+}
+
+// E4M3 weights: SwiGLU bf16 layer, rows of 16 bytes for the E4M3 maps.
+int validate_fp8(const moe_config* c, const void* w_gate, const void* w_up, const void* w_down,
+                 const float* scales) {
+  int st = moe_validate_config(c);
+  if (st != MOE_OK) return st;
+  if (c->dtype != MOE_BF16 || c->act != MOE_ACT_SWIGLU || c->has_ffn_bias) return MOE_ERR_UNSUPPORTED;
+  if (c->d_model % 16 != 0 || c->d_ff % 16 != 0) return MOE_ERR_INVALID_ARG;
+  if (!w_gate || !w_up || !w_down || !scales || !aligned16(w_up) || !aligned16(scales))
+    return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
 }
 
 }  // namespace
@@ -206,6 +270,7 @@ int moe_validate_config(const moe_config* c) {
   if (c->cap_mode < MOE_CAP_NONE || c->cap_mode > MOE_CAP_REROUTE) return MOE_ERR_INVALID_ARG;
   if (c->cap_mode != MOE_CAP_NONE && !(c->alpha > 0.f && isfinite(c->alpha)))
     return MOE_ERR_INVALID_ARG;
+  if (c->bias_mode != MOE_BIAS_LOGIT && c->bias_mode != MOE_BIAS_SELECT) return MOE_ERR_INVALID_ARG;
   if (c->has_ffn_bias && c->act != MOE_ACT_GELU) return MOE_ERR_UNSUPPORTED;
   if (c->dtype == MOE_BF16 && (c->act == MOE_ACT_GELU || c->has_ffn_bias)) return MOE_ERR_UNSUPPORTED;
   if (max_total_rows_of(c) >= INT32_MAX) return MOE_ERR_INVALID_ARG;
@@ -264,6 +329,21 @@ int moe_route(const moe_config* c, const void* x, const void* w_router, const fl
   return route_impl(c, x, w_router, bias, topk_idx, topk_w, probs, stats, ws, s);
 }
 
+int moe_router_bias_update(const moe_config* c, const void* ws, size_t ws_bytes, float* bias,
+                           float gamma, void* stream) {
+  int st = moe_validate_config(c);
+  if (st != MOE_OK) return st;
+  if ((st = check_ws(c, ws, ws_bytes)) != MOE_OK) return st;
+  if (!bias || !aligned16(bias) || !isfinite(gamma)) return MOE_ERR_INVALID_ARG;
+  if (c->n_tokens == 0) return MOE_OK;
+  const Layout L = layout_of(c);
+  return launch_bias_update(at<const int>(const_cast<void*>(ws), L.acc_pick), bias, c->n_tokens,
+                            c->n_experts, c->top_k, gamma, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
 int moe_dispatch(const moe_config* c, const int32_t* topk_idx, const float* probs, const void* x,
                  int32_t* final_idx, int32_t* pos, int32_t* offsets, int32_t* perm, void* x_perm,
                  const moe_stats* stats, void* ws, size_t ws_bytes, void* stream) {
@@ -293,7 +373,7 @@ int moe_expert_ffn(const moe_config* c, const void* x, const void* x_perm, const
       !aligned16(y_perm) || (w_up && !aligned16(w_up)))
     return MOE_ERR_INVALID_ARG;
   if (c->n_tokens == 0) return MOE_OK;
-  return ffn_impl(c, x, x_perm, offsets, counts, w_gate, w_up, w_down, b1, b2, y_perm, ws,
+  return ffn_impl(c, x, x_perm, offsets, counts, w_gate, w_up, w_down, b1, b2, nullptr, y_perm, ws,
                   static_cast<cudaStream_t>(stream), nullptr);
 }
 
@@ -315,44 +395,46 @@ int moe_forward(const moe_config* c, const void* x, const void* w_router, const 
                 void* stream, const moe_timing* timing) {
   int st = moe_validate_config(c);
   if (st != MOE_OK) return st;
-  if ((st = check_ws(c, ws, ws_bytes)) != MOE_OK) return st;
-  if (!x || !w_router || !w_gate || !w_down || !y) return MOE_ERR_INVALID_ARG;
   if (c->act == MOE_ACT_SWIGLU && !w_up) return MOE_ERR_INVALID_ARG;
-  if (c->has_router_bias && !bias) return MOE_ERR_INVALID_ARG;
   if (c->has_ffn_bias && (!b1 || !b2)) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(w_router) || !aligned16(w_gate) || !aligned16(w_down) ||
-      !aligned16(y) || (w_up && !aligned16(w_up)))
+  return forward_impl(c, x, w_router, bias, w_gate, w_up, w_down, b1, b2, nullptr, y, stats, ws,
+                      ws_bytes, stream, timing);
+}
+
+int moe_quantize_fp8(const void* w, int32_t n_mat, int64_t rows, int64_t cols, uint8_t* q,
+                     float* scales, void* stream) {
+  if (!w || !q || !scales || !aligned16(w) || !aligned16(q) || !aligned16(scales))
     return MOE_ERR_INVALID_ARG;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const Layout L = layout_of(c);
-  if (cudaMemsetAsync(ws, 0, L.zero_end, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (n_mat < 1 || n_mat > 65535 || rows < 1 || cols < 1 || (rows * cols) % 16 != 0)
+    return MOE_ERR_INVALID_ARG;
+  return launch_quantize_fp8(w, n_mat, rows * cols, q, scales, num_sms(),
+                             static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
+int moe_expert_ffn_fp8(const moe_config* c, const void* x, const void* x_perm,
+                       const int32_t* offsets, const int32_t* counts, const uint8_t* w_gate,
+                       const uint8_t* w_up, const uint8_t* w_down, const float* scales,
+                       void* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  int st = validate_fp8(c, w_gate, w_up, w_down, scales);
+  if (st != MOE_OK) return st;
+  if ((st = check_ws(c, ws, ws_bytes)) != MOE_OK) return st;
+  if (!x || !x_perm || !offsets || !counts || !y_perm) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x_perm) || !aligned16(y_perm)) return MOE_ERR_INVALID_ARG;
   if (c->n_tokens == 0) return MOE_OK;
-  float* probs = c->cap_mode == MOE_CAP_REROUTE ? at<float>(ws, L.probs) : nullptr;
-  record(timing, 0, s);
-  st = route_impl(c, x, w_router, bias, at<int32_t>(ws, L.topk_idx), at<float>(ws, L.topk_w),
-                  probs, stats, ws, s);
+  return ffn_impl(c, x, x_perm, offsets, counts, w_gate, w_up, w_down, nullptr, nullptr, scales,
+                  y_perm, ws, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+int moe_forward_fp8(const moe_config* c, const void* x, const void* w_router, const float* bias,
+                    const uint8_t* w_gate, const uint8_t* w_up, const uint8_t* w_down,
+                    const float* scales, void* y, const moe_stats* stats, void* ws,
+                    size_t ws_bytes, void* stream, const moe_timing* timing) {
+  const int st = validate_fp8(c, w_gate, w_up, w_down, scales);
   if (st != MOE_OK) return st;
-  record(timing, 1, s);
-  // the expert GEMMs read the per-expert counts: the caller's array when given
-  moe_stats st_fwd{};
-  if (stats) st_fwd = *stats;
-  if (!st_fwd.counts) st_fwd.counts = at<int32_t>(ws, L.counts);
-  st = dispatch_impl(c, at<int32_t>(ws, L.topk_idx), probs, x, at<int32_t>(ws, L.final_idx),
-                     at<int32_t>(ws, L.pos), at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.perm),
-                     at<void>(ws, L.x_perm), &st_fwd, ws, s);
-  if (st != MOE_OK) return st;
-  record(timing, 2, s);
-  st = ffn_impl(c, x, at<void>(ws, L.x_perm), at<int32_t>(ws, L.offsets), st_fwd.counts, w_gate,
-                w_up, w_down, b1, b2, at<void>(ws, L.y_perm), ws, s,
-                timing ? static_cast<cudaEvent_t>(timing->events[3]) : nullptr);
-  if (st != MOE_OK) return st;
-  record(timing, 4, s);
-  st = combine_impl(c, at<void>(ws, L.y_perm), at<int32_t>(ws, L.offsets),
-                    at<int32_t>(ws, L.final_idx), at<int32_t>(ws, L.pos), at<float>(ws, L.topk_w),
-                    y, s);
-  if (st != MOE_OK) return st;
-  record(timing, 5, s);
-  return MOE_OK;
+  return forward_impl(c, x, w_router, bias, w_gate, w_up, w_down, nullptr, nullptr, scales, y,
+                      stats, ws, ws_bytes, stream, timing);
 }
 
 int moe_device_status(void* ws, void* stream, int32_t* status_out) {

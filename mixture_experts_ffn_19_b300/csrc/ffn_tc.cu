@@ -25,6 +25,8 @@
 #include <mutex>
 
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -268,20 +270,40 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ 
 // which form silu(g)*u and store H.  GEMM-2 takes 128 rows of W_down per tile.
 // Tiles walk segment by segment, feature block by feature block, token chunk
 // fastest, so a weight tile is read from HBM once.
+//
+// FP8 weights (W8): the weight tile arrives as E4M3 codes (8 KB per stage, half
+// the HBM bytes) in a staging buffer; four converter warps widen it to bf16 in
+// the 128-byte-swizzled layout the MMA reads (every E4M3 value is exact in
+// bf16) and release the stage to the MMA warp; the per-expert-matrix scales
+// multiply the accumulators in the epilogue («大模型MoE架构揭秘» §5.4: expert
+// weights in low precision with per-expert scales, router in high precision).
 
 namespace swp {
 
 constexpr int BM = 128, TOK = 64, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = TOK * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int STAGES = 8;
+constexpr int A8_BYTES = BM * BK;              // E4M3 weight tile (W8 staging)
 constexpr int TMEM_COLS = 128;                 // two 64-column accumulators
 constexpr int XS = TOK + 1;                    // exchange row (floats), conflict-free
+constexpr int MAX_STAGES = 8;
+
+#ifndef MOE_FP8_CONV_WARPS
+#define MOE_FP8_CONV_WARPS 4
+#endif
+constexpr int CONV_WARPS = MOE_FP8_CONV_WARPS;     // converter warps (W8), from warp 6
+
+template <bool W8>
+struct Shape {
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + (W8 ? A8_BYTES : 0);
+  static constexpr int STAGES = W8 ? 6 : 8;
+  static constexpr int THREADS = W8 ? 192 + 32 * CONV_WARPS : 192;
+};
 
 struct Ctrl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
+  uint64_t conv[MAX_STAGES];     // W8: bf16 weight tile written
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t xfull;                // up values written to the exchange buffer
@@ -294,7 +316,11 @@ struct Ctrl {
 };
 
 constexpr size_t XCH_BYTES = (size_t)64 * XS * 4;
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + XCH_BYTES + sizeof(Ctrl);
+template <bool W8>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)Shape<W8>::STAGES * Shape<W8>::STAGE_BYTES + XCH_BYTES + sizeof(Ctrl);
+}
+static_assert(smem_bytes<true>() <= 232448 && smem_bytes<false>() <= 232448, "shared memory");
 
 struct Params {
   int E, S, N, K, n_out, n_fb;   // n_fb: feature blocks per segment
@@ -302,19 +328,39 @@ struct Params {
   const int32_t* counts;         // [E] valid rows of the routed segments
   __nv_bfloat16* out;
   int* status;
+  const float* scale0;           // W8: per-segment scales of the gate (GEMM-1) / down weights
+  const float* scale1;           // W8: per-segment scales of the up weights (GEMM-1)
 };
+
+// 8 E4M3 codes -> 8 bf16 (exact: E4M3 -> f16 -> f32 -> bf16 never rounds).
+// The conversion unit does it in four instructions per pair; integer bit
+// moves measured slower on this part.
+__device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint2 v) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t word = i < 2 ? v.x : v.y;
+    const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((word >> (16 * (i & 1))) & 0xFFFFu);
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+    const __nv_bfloat162 b = __float22bfloat162_rn(f);
+    w[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
 
 __device__ __forceinline__ int seg_rows(const Params& p, int s) {
   return s < p.E ? p.counts[s] : p.N;
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <int MODE, bool W8>
+__global__ void __launch_bounds__(Shape<W8>::THREADS, 1)
 ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                    const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    Params p) {
   // tmB0/tmB1: token rows (x_perm / x for GEMM-1, H for GEMM-2);
-  // tmA0/tmA1: weights (gate / up for GEMM-1, down for GEMM-2)
+  // tmA0/tmA1: weights (gate / up for GEMM-1, down for GEMM-2), bf16 or E4M3
+  constexpr int STAGES = Shape<W8>::STAGES, STAGE_BYTES = Shape<W8>::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -324,7 +370,11 @@ ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_consta
   const int nseg = p.E + p.S;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) { mbar_init(&ctrl->full[s], 1); mbar_init(&ctrl->empty[s], 1); }
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&ctrl->full[s], 1);
+      mbar_init(&ctrl->empty[s], 1);
+      mbar_init(&ctrl->conv[s], 32 * CONV_WARPS);
+    }
     for (int b = 0; b < 2; ++b) { mbar_init(&ctrl->tfull[b], 1); mbar_init(&ctrl->tempty[b], 128); }
     mbar_init(&ctrl->xfull, 64);
     mbar_init(&ctrl->xempty, 64);
@@ -379,12 +429,15 @@ ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_consta
           const uint32_t ph = (kc / STAGES) & 1;
           if (!mbar_wait(&ctrl->empty[st], ph ^ 1, abort, p.status)) break;
           uint8_t* a_s = smem + (size_t)st * STAGE_BYTES;
-          mbar_arrive_expect_tx(&ctrl->full[st], STAGE_BYTES);
+          // W8: the E4M3 weight tile goes to the staging buffer after B
+          uint8_t* w_s = W8 ? a_s + A_BYTES + B_BYTES : a_s;
+          const int half = W8 ? A8_BYTES / 2 : A_BYTES / 2;
+          mbar_arrive_expect_tx(&ctrl->full[st], W8 ? A8_BYTES + B_BYTES : STAGE_BYTES);
           if (MODE == 0) {
-            tma_load_2d(a_s, &tmA0, &ctrl->full[st], kb * BK, a_row);
-            tma_load_2d(a_s + A_BYTES / 2, &tmA1, &ctrl->full[st], kb * BK, a_row);
+            tma_load_2d(w_s, &tmA0, &ctrl->full[st], kb * BK, a_row);
+            tma_load_2d(w_s + half, &tmA1, &ctrl->full[st], kb * BK, a_row);
           } else {
-            tma_load_2d(a_s, &tmA0, &ctrl->full[st], kb * BK, a_row);
+            tma_load_2d(w_s, &tmA0, &ctrl->full[st], kb * BK, a_row);
           }
           tma_load_2d(a_s + A_BYTES, bmap, &ctrl->full[st], kb * BK, b_row);
         }
@@ -406,7 +459,7 @@ ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_consta
         for (int kb = 0; kb < KB; ++kb, ++kc) {
           const int st = kc % STAGES;
           const uint32_t ph = (kc / STAGES) & 1;
-          if (!mbar_wait(&ctrl->full[st], ph, abort, p.status)) { ok = false; break; }
+          if (!mbar_wait(W8 ? &ctrl->conv[st] : &ctrl->full[st], ph, abort, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + (size_t)st * STAGE_BYTES);
           const uint64_t adesc = sdesc_kmajor_sw128(a_addr);
@@ -420,7 +473,40 @@ ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_consta
         umma_commit(&ctrl->tfull[buf]);
       }
     }
-  } else {
+  } else if (W8 && warp >= 6 && warp < 6 + CONV_WARPS) {
+    // converter warps: E4M3 staging tile -> bf16 tile in the 128-byte swizzled
+    // K-major layout (16-byte chunk c of row r at chunk c ^ (r & 7)); 8 threads
+    // per row, 4 * CONV_WARPS rows per pass
+    constexpr int ROWS_PER_PASS = 4 * CONV_WARPS;
+    const int ct = threadIdx.x - 192;
+    uint32_t kc = 0;
+    for (int T = blockIdx.x; T < total_tiles && !*abort; T += gridDim.x) {
+      bool ok = true;
+      for (int kb = 0; kb < KB; ++kb, ++kc) {
+        const int st = kc % STAGES;
+        const uint32_t ph = (kc / STAGES) & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&ctrl->full[st], ph, abort, p.status))) { ok = false; break; }
+        uint8_t* a_s = smem + (size_t)st * STAGE_BYTES;
+        const uint8_t* w_s = a_s + A_BYTES + B_BYTES;
+        // all of this thread's codes first (their loads in flight together),
+        // then the conversions and swizzled stores
+        constexpr int PASSES = BM / ROWS_PER_PASS;
+        const int c = ct & 7;
+        uint2 v[PASSES];
+#pragma unroll
+        for (int pass = 0; pass < PASSES; ++pass)
+          v[pass] = *reinterpret_cast<const uint2*>(w_s + (pass * ROWS_PER_PASS + (ct >> 3)) * BK + c * 8);
+#pragma unroll
+        for (int pass = 0; pass < PASSES; ++pass) {
+          const int r = pass * ROWS_PER_PASS + (ct >> 3);
+          *reinterpret_cast<uint4*>(a_s + r * 128 + ((c ^ (r & 7)) << 4)) = e4m3x8_to_bf16x8(v[pass]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&ctrl->conv[st]);
+      }
+      if (!ok) break;
+    }
+  } else if (warp >= 2 && warp < 6) {
     const int q = warp & 3;                      // TMEM lanes 32q .. 32q+31 = weight rows
     uint32_t it = 0;
     for (int T = blockIdx.x; T < total_tiles; T += gridDim.x, ++it) {
@@ -444,12 +530,13 @@ ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_consta
         if (q >= 2) {
           xok = mbar_wait(&ctrl->xempty, (it & 1) ^ 1, abort, p.status);
           if (__all_sync(0xffffffffu, xok)) {
+            const float su = W8 ? p.scale1[seg] : 1.f;
             for (int c = 0; c < ncc; ++c) {
               uint32_t u[32];
               tmem_ld32(taddr + c * 32, u);
               tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 32; ++i) xch[f * XS + c * 32 + i] = __uint_as_float(u[i]);
+              for (int i = 0; i < 32; ++i) xch[f * XS + c * 32 + i] = __uint_as_float(u[i]) * su;
             }
             mbar_arrive(&ctrl->xfull);
           }
@@ -459,6 +546,7 @@ ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_consta
         if (!__all_sync(0xffffffffu, xok)) break;
         if (q < 2) {
           const int col = fb * 64 + f;
+          const float sg = W8 ? p.scale0[seg] : 1.f;
           for (int c = 0; c < ncc; ++c) {
             uint32_t g[32];
             tmem_ld32(taddr + c * 32, g);
@@ -468,7 +556,7 @@ ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_consta
               for (int i = 0; i < 32; ++i) {
                 const int t = c * 32 + i;
                 if (t < nt) {
-                  const float h = silu_f(__uint_as_float(g[i])) * xch[f * XS + t];
+                  const float h = silu_f(__uint_as_float(g[i]) * sg) * xch[f * XS + t];
                   p.out[(size_t)(row0 + t) * p.n_out + col] = __float2bfloat16_rn(h);
                 }
               }
@@ -478,6 +566,7 @@ ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_consta
         }
       } else {
         const int col = fb * BM + q * 32 + lane;
+        const float sd = W8 ? p.scale0[seg] : 1.f;
         for (int c = 0; c < ncc; ++c) {
           uint32_t y[32];
           tmem_ld32(taddr + c * 32, y);
@@ -486,7 +575,7 @@ ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_consta
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const int t = c * 32 + i;
-              if (t < nt) p.out[(size_t)(row0 + t) * p.n_out + col] = __float2bfloat16_rn(__uint_as_float(y[i]));
+              if (t < nt) p.out[(size_t)(row0 + t) * p.n_out + col] = __float2bfloat16_rn(__uint_as_float(y[i]) * sd);
             }
           }
         }
@@ -535,44 +624,67 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D E4M3 map over a row-major [rows, cols] byte matrix, box [box_rows, 64],
+// no swizzle (the converter warps lay the bf16 tile out themselves).
+bool make_map8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {BK, box_rows};
+  const cuuint32_t elem[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                  box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 namespace {
 
 // Swap-AB (weights as the M operand) when experts see few tokens: decode-sized
-// batches, where 128-row token tiles would be mostly padding.
+// batches, where 128-row token tiles would be mostly padding.  E4M3 weights
+// always take this kernel (it handles any number of tokens per expert).
 bool use_swap(const FfnParams& p) {
+  if (p.w_scales) return true;
   if (!p.counts) return false;
   if ((int64_t)p.N * p.k > 64LL * p.E) return false;
   return p.S == 0 || p.N <= 512;
 }
 
+template <bool W8>
 cudaError_t launch_swap(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) {
-  cudaError_t err = cudaFuncSetAttribute(swp::ffn_tc_swap_kernel<0>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)swp::SMEM_BYTES);
+  constexpr size_t SMEM = swp::smem_bytes<W8>();
+  constexpr int THREADS = swp::Shape<W8>::THREADS;
+  cudaError_t err = cudaFuncSetAttribute(swp::ffn_tc_swap_kernel<0, W8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
   if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(swp::ffn_tc_swap_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)swp::SMEM_BYTES);
+  err = cudaFuncSetAttribute(swp::ffn_tc_swap_kernel<1, W8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM);
   if (err != cudaSuccess) return err;
   const int ET = p.E + p.S;
+  auto wmap = [&](CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box) {
+    return W8 ? make_map8(m, base, rows, cols, box) : make_map(m, base, rows, cols, box);
+  };
   CUtensorMap b0, b1, a0, a1;
   if (!make_map(&b0, p.x_perm, (uint64_t)p.max_rows, p.d, swp::TOK) ||
       !make_map(&b1, p.x, (uint64_t)p.N, p.d, swp::TOK) ||
-      !make_map(&a0, p.w_gate, (uint64_t)ET * p.F, p.d, swp::BM / 2) ||
-      !make_map(&a1, p.w_up, (uint64_t)ET * p.F, p.d, swp::BM / 2))
+      !wmap(&a0, p.w_gate, (uint64_t)ET * p.F, p.d, swp::BM / 2) ||
+      !wmap(&a1, p.w_up, (uint64_t)ET * p.F, p.d, swp::BM / 2))
     return cudaErrorInvalidValue;
   swp::Params t1{p.E, p.S, p.N, p.d, p.F, (p.F + 63) / 64, p.offsets, p.counts,
-            static_cast<__nv_bfloat16*>(p.h), p.status};
-  swp::ffn_tc_swap_kernel<0><<<p.num_sms, NUM_THREADS, swp::SMEM_BYTES, s>>>(b0, b1, a0, a1, t1);
+                 static_cast<__nv_bfloat16*>(p.h), p.status,
+                 W8 ? p.w_scales : nullptr, W8 ? p.w_scales + ET : nullptr};
+  swp::ffn_tc_swap_kernel<0, W8><<<p.num_sms, THREADS, SMEM, s>>>(b0, b1, a0, a1, t1);
   count_launch();
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   if (mid) cudaEventRecord(mid, s);
   if (!make_map(&b0, p.h, (uint64_t)p.max_total_rows, p.F, swp::TOK) ||
-      !make_map(&a0, p.w_down, (uint64_t)ET * p.d, p.F, swp::BM))
+      !wmap(&a0, p.w_down, (uint64_t)ET * p.d, p.F, swp::BM))
     return cudaErrorInvalidValue;
   swp::Params t2{p.E, p.S, p.N, p.F, p.d, (p.d + swp::BM - 1) / swp::BM, p.offsets, p.counts,
-            static_cast<__nv_bfloat16*>(p.y_perm), p.status};
-  swp::ffn_tc_swap_kernel<1><<<p.num_sms, NUM_THREADS, swp::SMEM_BYTES, s>>>(b0, b0, a0, a0, t2);
+                 static_cast<__nv_bfloat16*>(p.y_perm), p.status,
+                 W8 ? p.w_scales + 2 * ET : nullptr, nullptr};
+  swp::ffn_tc_swap_kernel<1, W8><<<p.num_sms, THREADS, SMEM, s>>>(b0, b0, a0, a0, t2);
   count_launch();
   return cudaGetLastError();
 }
@@ -620,7 +732,8 @@ cudaError_t launch_prefill(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) 
 cudaError_t launch_ffn_tc(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) {
   cudaError_t err = get_encoder();
   if (err != cudaSuccess) return err;
-  if (use_swap(p)) return launch_swap(p, s, mid);
+  if (p.w_scales) return launch_swap<true>(p, s, mid);
+  if (use_swap(p)) return launch_swap<false>(p, s, mid);
   return launch_prefill<Prefill>(p, s, mid);
 }
 

@@ -17,6 +17,7 @@ struct RouteParams {
   const void* x;             // [N, d]
   const void* w_router;      // [E, d]
   const float* bias;         // [E] or null
+  int bias_select;           // 1: the bias only steers the top-k (p + b)
   int N, d, E, k;
   int32_t* topk_idx;         // [N, k]
   float* topk_w;             // [N, k]
@@ -28,11 +29,21 @@ struct RouteParams {
   unsigned long long* acc_p; // [E]
   int* acc_pick;             // [E]
   unsigned* ticket;          // [1]
+  // z-loss and entropy: sums of lse^2 (2^-24 units) and of H (2^-40 units)
+  unsigned long long* acc_zh; // [2]
   float* expert_freq;        // [E]
   float* mean_prob;          // [E]
   float* l_bal;              // [1]
+  float* z_loss;             // [1]
+  float* entropy;            // [1]
   int* status;
 };
+
+cudaError_t launch_quantize_fp8(const void* w, int n_mat, int64_t per_mat, uint8_t* q, float* scales,
+                                int num_sms, cudaStream_t s);
+
+cudaError_t launch_bias_update(const int* picks, float* bias, int N, int E, int k, float gamma,
+                               cudaStream_t s);
 
 // Split of the router contraction over K: ks slices of k_slice (a multiple of 64).
 struct RouteSplit {
@@ -97,6 +108,9 @@ struct FfnParams {
   int64_t max_rows, max_total_rows;
   int* status;
   int num_sms;
+  // E4M3 weights: w_gate / w_up / w_down hold codes and w_scales [3][E+S] the
+  // gate, up and down scale of each expert; null for bf16 weights
+  const float* w_scales;
 };
 
 struct CombineParams {

@@ -124,26 +124,38 @@ template <int EJ>
 __global__ void __launch_bounds__(kThreads) route_finish_kernel(RouteParams p, RouteSplit sp) {
   constexpr int EP = EJ * 32;
   __shared__ unsigned long long psum_w[kWarps][EP];
+  __shared__ unsigned long long zh_w[kWarps][2];
   __shared__ int picks_s[EP];
   __shared__ bool last_cta;
   const int E = p.E, N = p.N, k = p.k;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // bias on the logits (before the softmax) or on the selection key only
+  const bool bias_logit = p.bias && !p.bias_select, bias_sel = p.bias && p.bias_select;
   for (int e = tid; e < EP; e += kThreads) picks_s[e] = 0;
   __syncthreads();
   unsigned long long psum[EJ];                  // sum of p in units of 2^-40 (exact)
 #pragma unroll
   for (int c = 0; c < EJ; ++c) psum[c] = 0ull;
+  unsigned long long zacc = 0ull, hacc = 0ull;  // lane 0: lse^2 (2^-20), H (2^-40)
+  float b[EJ];                                  // this lane's bias values
+#pragma unroll
+  for (int c = 0; c < EJ; ++c) {
+    const int e = lane + 32 * c;
+    b[c] = (p.bias && e < E) ? p.bias[e] : 0.f;
+  }
   const int tpw = route_finish_tpw(N);
   for (int i = 0; i < tpw; ++i) {
     const int t = (blockIdx.x * kWarps + warp) * tpw + i;
     if (t >= N) break;
-    float v[EJ];
-    float m = -INFINITY;
+    float v[EJ], raw[EJ];
+    float m = -INFINITY, mr = -INFINITY;
 #pragma unroll
     for (int c = 0; c < EJ; ++c) {
       const int e = lane + 32 * c;
-      v[c] = (e < E) ? p.part[(size_t)t * E + e] + (p.bias ? p.bias[e] : 0.f) : -INFINITY;
+      raw[c] = (e < E) ? p.part[(size_t)t * E + e] : -INFINITY;
+      v[c] = (e < E) ? raw[c] + (bias_logit ? b[c] : 0.f) : -INFINITY;
       m = fmaxf(m, v[c]);
+      mr = fmaxf(mr, raw[c]);
     }
     m = warp_max(m);
     float s = 0.f;
@@ -153,44 +165,76 @@ __global__ void __launch_bounds__(kThreads) route_finish_kernel(RouteParams p, R
       s += v[c];
     }
     s = warp_sum(s);
+    if (p.z_loss) {
+      // logsumexp of the bias-free logits («项目概述：为什么MoE...» §3.3)
+      float lse;
+      if (bias_logit) {
+        mr = warp_max(mr);
+        float sr = 0.f;
+#pragma unroll
+        for (int c = 0; c < EJ; ++c) sr += (lane + 32 * c < E) ? expf(raw[c] - mr) : 0.f;
+        lse = mr + logf(warp_sum(sr));
+      } else {
+        lse = m + logf(s);
+      }
+      if (lane == 0) zacc += __float2ull_rn(lse * lse * 1048576.0f);
+    }
+    float key[EJ];   // what the top-k ranks: p, or p + b under selection-only bias
 #pragma unroll
     for (int c = 0; c < EJ; ++c) {
       const int e = lane + 32 * c;
       v[c] = v[c] / s;
+      key[c] = bias_sel ? v[c] + b[c] : v[c];
       if (e < E) {
         psum[c] += __float2ull_rn(v[c] * 1099511627776.0f);
-        if (p.probs) p.probs[(size_t)t * E + e] = v[c];
+        if (p.probs) p.probs[(size_t)t * E + e] = key[c];
       }
     }
     uint32_t taken = 0;
     float ksum = 0.f, my_p = 0.f;
     int my_e = 0;
     for (int q = 0; q < k; ++q) {
-      float bp = -1.f;
+      float bk = -INFINITY;
       int be = 0x7fffffff;
 #pragma unroll
       for (int c = 0; c < EJ; ++c) {
         const int e = lane + 32 * c;
-        if (e < E && !((taken >> c) & 1u) && better(v[c], e, bp, be)) { bp = v[c]; be = e; }
+        if (e < E && !((taken >> c) & 1u) && better(key[c], e, bk, be)) { bk = key[c]; be = e; }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
-        const float op = __shfl_xor_sync(0xffffffffu, bp, o);
+        const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
         const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (better(op, oe, bp, be)) { bp = op; be = oe; }
+        if (better(ok, oe, bk, be)) { bk = ok; be = oe; }
+      }
+      // the winner's probability (its key, unless the bias steered the choice)
+      float pw = bk;
+      if (bias_sel) {
+        float mine = 0.f;
+#pragma unroll
+        for (int c = 0; c < EJ; ++c)
+          if (c == (be >> 5)) mine = v[c];
+        pw = __shfl_sync(0xffffffffu, mine, be & 31);
       }
       if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (q == lane) { my_p = bp; my_e = be; }
-      ksum += bp;
+      if (q == lane) { my_p = pw; my_e = be; }
+      ksum += pw;
     }
+    const float my_w = my_p / ksum;
     if (lane < k) {
       p.topk_idx[(size_t)t * k + lane] = my_e;
-      p.topk_w[(size_t)t * k + lane] = my_p / ksum;
+      p.topk_w[(size_t)t * k + lane] = my_w;
       atomicAdd(&picks_s[my_e], 1);
+    }
+    if (p.entropy) {
+      // -sum_j w_j log2 w_j over the gates («GPT-4 Has 1.8 Trillion ...» §2.3)
+      const float h = warp_sum((lane < k && my_w > 0.f) ? -my_w * log2f(my_w) : 0.f);
+      if (lane == 0) hacc += __float2ull_rn(h * 1099511627776.0f);
     }
   }
 #pragma unroll
   for (int c = 0; c < EJ; ++c) psum_w[warp][lane + 32 * c] = psum[c];
+  if (lane == 0) { zh_w[warp][0] = zacc; zh_w[warp][1] = hacc; }
   __syncthreads();
   // integer sums are exact, so the cross-CTA atomics are order-independent
   for (int e = tid; e < E; e += kThreads) {
@@ -198,6 +242,11 @@ __global__ void __launch_bounds__(kThreads) route_finish_kernel(RouteParams p, R
     for (int w = 0; w < kWarps; ++w) acc += psum_w[w][e];
     atomicAdd(&p.acc_p[e], acc);
     atomicAdd(&p.acc_pick[e], picks_s[e]);
+  }
+  if (tid < 2 && (tid == 0 ? p.z_loss != nullptr : p.entropy != nullptr)) {
+    unsigned long long acc = 0ull;
+    for (int w = 0; w < kWarps; ++w) acc += zh_w[w][tid];
+    atomicAdd(&p.acc_zh[tid], acc);
   }
   __threadfence();
   __syncthreads();
@@ -220,6 +269,20 @@ __global__ void __launch_bounds__(kThreads) route_finish_kernel(RouteParams p, R
     for (int e = 0; e < E; ++e) s.add(contrib[e]);
     p.l_bal[0] = (float)E * s.s;
   }
+  if (tid == 32 && p.z_loss)
+    p.z_loss[0] = (float)(0.001 * (__ull2double_rn(__ldcg(&p.acc_zh[0])) / 1048576.0) / N);
+  if (tid == 64 && p.entropy)
+    p.entropy[0] = (float)(__ull2double_rn(__ldcg(&p.acc_zh[1])) / 1099511627776.0 / N);
+}
+
+// Auxiliary-loss-free balancing step («为什么MoE有效？...» §2.4): lower the
+// bias of an expert that got more than N*k/E picks, raise it below that.
+__global__ void bias_update_kernel(const int* picks, float* bias, int N, int E, int k, float gamma) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  const long long load = (long long)picks[e] * E, mean = (long long)N * k;
+  if (load > mean) bias[e] = bias[e] - gamma;
+  else if (load < mean) bias[e] = bias[e] + gamma;
 }
 
 // Logits from the K-slice partials: part[0][t][e] = sum_s part[s][t][e], a
@@ -297,6 +360,13 @@ RouteSplit route_split(int N, int d, bool bf16) {
   r.k_slice = k_slice;
   r.ks = (d + k_slice - 1) / k_slice;
   return r;
+}
+
+cudaError_t launch_bias_update(const int* picks, float* bias, int N, int E, int k, float gamma,
+                               cudaStream_t s) {
+  bias_update_kernel<<<(E + 255) / 256, 256, 0, s>>>(picks, bias, N, E, k, gamma);
+  count_launch();
+  return cudaGetLastError();
 }
 
 cudaError_t launch_route(const RouteParams& p, bool bf16, cudaStream_t s) {

@@ -38,6 +38,7 @@ CAP_REROUTE = 2
 BIAS_NONE = "none"
 BIAS_UNIFORM = "uniform_0.1"     # expert_bias ~ U(-0.1, 0.1)
 BIAS_LOGZIPF = "logzipf_1.1"     # b[e] = -1.1 * ln(r_e), r a seeded permutation of 1..E
+BIAS_UNIFORM_P = "uniform_p"     # b ~ U(-1/(2E), 1/(2E)): half the mean probability
 
 
 @dataclasses.dataclass(frozen=True)
@@ -57,6 +58,7 @@ class Workload:
     bias_law: str
     seed: int
     bias_mode: int = 0          # 0: bias added to the logits, 1: selection only
+    fp8_weights: bool = False   # expert weights quantised to FP8 E4M3 by the library
 
     @property
     def has_router_bias(self) -> bool:
@@ -85,10 +87,19 @@ WORKLOADS = {
                                DT_BF16, CAP_NONE, 0.0, False, BIAS_LOGZIPF, 0x4D6F4505),
     "decode_dsv2": Workload("decode_dsv2", 32, 5120, 160, 6, 1536, 2, ACT_SWIGLU, DT_BF16,
                             CAP_NONE, 0.0, False, BIAS_LOGZIPF, 0x4D6F4506),
+    # The decode layers with FP8 E4M3 expert weights (same draws, quantised by
+    # the library with one scale per expert matrix).
+    "decode_mixtral_fp8": Workload("decode_mixtral_fp8", 64, 4096, 8, 2, 14336, 0, ACT_SWIGLU,
+                                   DT_BF16, CAP_NONE, 0.0, False, BIAS_LOGZIPF, 0x4D6F4505,
+                                   fp8_weights=True),
+    "decode_dsv2_fp8": Workload("decode_dsv2_fp8", 32, 5120, 160, 6, 1536, 2, ACT_SWIGLU, DT_BF16,
+                                CAP_NONE, 0.0, False, BIAS_LOGZIPF, 0x4D6F4506, fp8_weights=True),
     # The DeepSeek-V2-like layer with the bias steering selection only
-    # (DeepSeek-V3 style); same shapes and inputs as "dsv2".
+    # (DeepSeek-V3 style): same shapes and x / weights as "dsv2"; the bias is
+    # added to probabilities here, so it is drawn on their scale (a tilt that
+    # reorders close experts without overriding the router).
     "dsv2_select": Workload("dsv2_select", 8192, 5120, 160, 6, 1536, 2, ACT_SWIGLU, DT_BF16,
-                            CAP_NONE, 0.0, False, BIAS_UNIFORM, 0x4D6F4503, bias_mode=1),
+                            CAP_NONE, 0.0, False, BIAS_UNIFORM_P, 0x4D6F4503, bias_mode=1),
 }
 
 # Tensor identifiers inside one workload's seed space.
@@ -136,6 +147,9 @@ def router_bias(w: Workload) -> np.ndarray | None:
         return None
     if w.bias_law == BIAS_UNIFORM:
         return _rng(w.seed, _T_BIAS).uniform(-0.1, 0.1, size=E).astype(np.float32)
+    if w.bias_law == BIAS_UNIFORM_P:
+        h = 0.5 / E
+        return _rng(w.seed, _T_BIAS).uniform(-h, h, size=E).astype(np.float32)
     if w.bias_law == BIAS_LOGZIPF:
         # Zipf popularity over a seeded ranking of the experts: weight r^-s for the
         # expert of rank r; its log is -s*ln(r).  The normalising constant is dropped

@@ -10,7 +10,8 @@ import synth
 def config_of(w: synth.Workload) -> moe.moe_config:
     return moe.make_config(w.n_tokens, w.d_model, w.n_experts, w.top_k, w.d_ff, w.n_shared,
                            act=w.act, dtype=w.dtype, cap_mode=w.cap_mode, alpha=w.alpha,
-                           has_ffn_bias=w.has_ffn_bias, has_router_bias=w.has_router_bias)
+                           has_ffn_bias=w.has_ffn_bias, has_router_bias=w.has_router_bias,
+                           bias_mode=w.bias_mode)
 
 
 def to_dev(a, device="cuda"):
@@ -38,3 +39,41 @@ def rel_err_inf(y, ref):
 def segment_rows(offsets, counts, E):
     """Per-expert row ranges [offsets[e], offsets[e] + counts[e])."""
     return [(int(offsets[e]), int(offsets[e]) + int(counts[e])) for e in range(E)]
+
+
+def a128(n):
+    return (n + 127) // 128 * 128
+
+
+def host_layout(w, members):
+    """Segment offsets [E+S+1] for the given per-expert member lists (128-row padding)."""
+    E, S, N = w.n_experts, w.n_shared, w.n_tokens
+    offsets, row = [], 0
+    for e in range(E):
+        offsets.append(row)
+        row += a128(len(members[e]))
+    for s in range(S):
+        offsets.append(row)
+        row += a128(N)
+    offsets.append(row)
+    return np.array(offsets, dtype=np.int32)
+
+
+def upload_experts(w, device):
+    """Expert weights as device arrays [E+S, ...], drawn and copied one expert at a time."""
+    import concurrent.futures as cf
+    import torch
+    ET, F, d = w.n_experts + w.n_shared, w.d_ff, w.d_model
+    dt = torch.bfloat16 if w.dtype == synth.DT_BF16 else torch.float32
+    dev = {"w_gate": torch.empty((ET, F, d), dtype=dt, device=device),
+           "w_up": torch.empty((ET, F, d), dtype=dt, device=device)
+           if w.act == synth.ACT_SWIGLU else None,
+           "w_down": torch.empty((ET, d, F), dtype=dt, device=device),
+           "b1": torch.empty((ET, F), dtype=dt, device=device) if w.has_ffn_bias else None,
+           "b2": torch.empty((ET, d), dtype=dt, device=device) if w.has_ffn_bias else None}
+    with cf.ThreadPoolExecutor(8) as ex:
+        for e, r in zip(range(ET), ex.map(lambda e: synth.expert_weights(w, e), range(ET))):
+            for key, t in dev.items():
+                if t is not None:
+                    t[e].copy_(to_dev(r[key], device))
+    return dev

@@ -51,6 +51,8 @@ def test_validation(lib):
                              ("n_tokens", -1, moe.MOE_ERR_INVALID_ARG),
                              ("cap_mode", 3, moe.MOE_ERR_INVALID_ARG),
                              ("alpha", 0.0, moe.MOE_ERR_INVALID_ARG),
+                             ("bias_mode", 2, moe.MOE_ERR_INVALID_ARG),
+                             ("bias_mode", -1, moe.MOE_ERR_INVALID_ARG),
                              ("act", moe.MOE_ACT_GELU, moe.MOE_ERR_UNSUPPORTED)]:
         c = config_of(synth.WORKLOADS["mixtral_prefill"])
         setattr(c, field, bad)

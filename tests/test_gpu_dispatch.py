@@ -76,8 +76,9 @@ def check_dispatch(w, inp, idx, p, g):
 
 
 def routed(w, inp):
-    r = oracle.route(inp["x"], inp["w_router"], inp["router_bias"], w.top_k)
-    return r["idx"], r["p"]
+    # the reroute ranks candidates by the selection scores (p, or p + b)
+    r = oracle.route(inp["x"], inp["w_router"], inp["router_bias"], w.top_k, w.bias_mode)
+    return r["idx"], r["key"]
 
 
 CASES = [
@@ -91,6 +92,9 @@ CASES = [
     synth.small_workload("dsv2", n_tokens=333, d_model=64, n_experts=160, top_k=6, n_shared=2),
     synth.small_workload("dsv2", n_tokens=1, d_model=64),
     synth.small_workload("e64_reroute", n_tokens=2500, d_model=64, n_experts=256, top_k=8, alpha=1.0),
+    # reroute ranked by p + b (selection-only bias)
+    synth.small_workload("e64_reroute", n_tokens=1500, d_model=64, alpha=0.7,
+                         bias_law=synth.BIAS_UNIFORM_P, bias_mode=1),
 ]
 
 

@@ -7,32 +7,15 @@ import torch
 import mixture_experts_ffn_19_b300 as moe
 import oracle
 import synth
-from helpers import config_of, rel_err_inf, to_dev, to_f64
+from helpers import config_of, host_layout, rel_err_inf, to_dev, to_f64
 
 pytestmark = pytest.mark.gpu
 
 
-def a128(n):
-    return (n + 127) // 128 * 128
-
-
-def host_layout(w, members):
-    E, S, N = w.n_experts, w.n_shared, w.n_tokens
-    offsets, row = [], 0
-    for e in range(E):
-        offsets.append(row)
-        row += a128(len(members[e]))
-    for s in range(S):
-        offsets.append(row)
-        row += a128(N)
-    offsets.append(row)
-    return np.array(offsets, dtype=np.int32)
-
-
 def oracle_routing(w, inp):
-    r = oracle.route(inp["x"], inp["w_router"], inp["router_bias"], w.top_k)
+    r = oracle.route(inp["x"], inp["w_router"], inp["router_bias"], w.top_k, w.bias_mode)
     C = oracle.capacity(w.n_tokens, w.n_experts, w.top_k, w.alpha) if w.cap_mode else None
-    d = oracle.dispatch(r["idx"], r["p"], w.n_experts, w.cap_mode, C)
+    d = oracle.dispatch(r["idx"], r["key"], w.n_experts, w.cap_mode, C)
     return r, d
 
 

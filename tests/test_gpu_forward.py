@@ -82,6 +82,10 @@ SMALL = [
     synth.small_workload("mixtral_prefill", n_tokens=2048, d_model=256, n_experts=4, d_ff=320, alpha=1.0),
     synth.small_workload("dsv2", n_tokens=1600, d_model=192, n_experts=4, top_k=2, d_ff=192, n_shared=1),
     synth.small_workload("decode_dsv2", d_model=256, d_ff=256),
+    # selection-only bias (DeepSeek-V3 style), with and without reroute
+    synth.small_workload("dsv2_select", n_tokens=500, d_model=256, n_experts=32, top_k=4, d_ff=256),
+    synth.small_workload("e64_reroute", n_tokens=1500, d_model=256, d_ff=256, alpha=0.8,
+                         bias_law=synth.BIAS_UNIFORM_P, bias_mode=1),
 ]
 
 

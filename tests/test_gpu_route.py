@@ -23,31 +23,43 @@ def run_route(w, inp, device):
     freq = torch.zeros(E, dtype=torch.float32, device=device)
     mp = torch.zeros(E, dtype=torch.float32, device=device)
     lb = torch.zeros(1, dtype=torch.float32, device=device)
-    st = moe.make_stats(expert_freq=freq, mean_prob=mp, l_bal=lb)
+    zl = torch.full((1,), -1.0, dtype=torch.float32, device=device)
+    ent = torch.full((1,), -1.0, dtype=torch.float32, device=device)
+    st = moe.make_stats(expert_freq=freq, mean_prob=mp, l_bal=lb, z_loss=zl, router_entropy=ent)
     moe.moe_route(cfg, to_dev(inp["x"]), to_dev(inp["w_router"]), to_dev(inp["router_bias"]),
                   idx, gw, probs, st, ws)
     assert moe.moe_device_status(ws) == moe.MOE_OK
-    return {k_: v.cpu().numpy() for k_, v in
-            dict(idx=idx, w=gw, p=probs, freq=freq, mean_prob=mp, l_bal=lb).items()}
+    out = {k_: v.cpu().numpy() for k_, v in
+           dict(idx=idx, w=gw, p=probs, freq=freq, mean_prob=mp, l_bal=lb, z_loss=zl,
+                entropy=ent).items()}
+    out["ws"] = ws
+    return out
 
 
 def check_route(w, inp, g):
-    r = oracle.route(inp["x"], inp["w_router"], inp["router_bias"], w.top_k)
+    r = oracle.route(inp["x"], inp["w_router"], inp["router_bias"], w.top_k, w.bias_mode)
     near = r["margin"] < NEAR_TIE
     same = np.all(g["idx"] == r["idx"], axis=1)
     mism = np.nonzero(~same)[0]
     print(f"{w.name}: near-tie tokens {near.sum()}, index mismatches {len(mism)}, "
-          f"max |dp| {np.max(np.abs(g['p'] - r['p'])):.3g}")
+          f"max |dp| {np.max(np.abs(g['p'] - r['key'])):.3g}")
     # every mismatch must be a counted near-tie
     assert np.all(near[mism]), f"mismatch on non-near-tie tokens {mism[~near[mism]][:10]}"
     ok = same & ~near
     np.testing.assert_allclose(g["w"][ok], r["w"][ok], rtol=1e-5, atol=1e-7)
-    np.testing.assert_allclose(g["p"], r["p"], rtol=1e-5, atol=1e-7)
+    # probs holds the selection scores: p, or p + b under selection-only bias
+    np.testing.assert_allclose(g["p"], r["key"], rtol=1e-5, atol=1e-7)
     np.testing.assert_allclose(g["mean_prob"], r["mean_prob"], rtol=1e-5, atol=1e-9)
     if len(mism) == 0:
         np.testing.assert_array_equal(g["freq"], r["expert_freq"].astype(np.float32))
     np.testing.assert_allclose(g["l_bal"][0], r["l_bal"], rtol=1e-5)
     assert np.allclose(g["w"].astype(np.float64).sum(1), 1.0, atol=1e-6)
+    # z-loss (fp32 logsumexp per token); entropy (a flipped near-tie token may
+    # move its own term by at most log2 k)
+    np.testing.assert_allclose(g["z_loss"][0], r["z_loss"], rtol=2e-5)
+    tol = 1e-5 * r["router_entropy"] + len(mism) * np.log2(max(w.top_k, 2)) / w.n_tokens
+    assert abs(g["entropy"][0] - r["router_entropy"]) <= tol + 1e-7
+    return r
 
 
 SMALL = [
@@ -57,6 +69,9 @@ SMALL = [
     synth.small_workload("e64_reroute", n_tokens=1000, d_model=256),
     synth.small_workload("mixtral_prefill", n_tokens=1, d_model=64, n_experts=1, top_k=1),
     synth.small_workload("dsv2", n_tokens=129, d_model=64, n_experts=256, top_k=8),
+    # selection-only bias (DeepSeek-V3 style), fp32 and bf16
+    synth.small_workload("dsv2_select", n_tokens=700, d_model=256, n_experts=64, top_k=6),
+    synth.small_workload("tiny_fp32", n_tokens=150, bias_law=synth.BIAS_UNIFORM_P, bias_mode=1),
 ]
 
 
@@ -83,3 +98,57 @@ def test_zero_router_uniform(cuda):
     assert np.all(g["idx"] == np.arange(2)[None, :])          # ties -> lowest indices
     assert g["l_bal"][0] == 1.0
     assert np.all(g["p"] == np.float32(1 / 64))
+
+
+def test_z_loss_entropy_closed_form(cuda):
+    # zero router: lse = ln E for every token, equal gates give log2 k bits
+    w = synth.small_workload("e64_reroute", n_tokens=300, d_model=64, top_k=4)
+    inp = synth.make_inputs(w, with_experts=False)
+    inp["w_router"][:] = 0
+    inp["router_bias"] = None
+    w = w.replace(bias_law=synth.BIAS_NONE)
+    g = run_route(w, inp, cuda)
+    np.testing.assert_allclose(g["z_loss"][0], 0.001 * np.log(64) ** 2, rtol=1e-6)
+    np.testing.assert_allclose(g["entropy"][0], 2.0, rtol=1e-6)
+
+
+@pytest.mark.parametrize("w", [
+    synth.small_workload("dsv2_select", n_tokens=700, d_model=256, n_experts=64, top_k=6),
+    synth.small_workload("e64_reroute", n_tokens=1000, d_model=256),
+    synth.small_workload("mixtral_prefill", n_tokens=0, d_model=64),
+], ids=lambda w: f"{w.name}-N{w.n_tokens}")
+def test_router_bias_update(cuda, w):
+    """b_e -/+ gamma from the picks of the last route on the workspace."""
+    inp = synth.make_inputs(w, with_experts=False)
+    if inp["router_bias"] is None:
+        inp["router_bias"] = np.zeros(w.n_experts, dtype=np.float32)
+        w = w.replace(bias_law=synth.BIAS_UNIFORM_P)
+    cfg = config_of(w)
+    g = run_route(w, inp, cuda) if w.n_tokens else {"ws": moe.alloc_workspace(cfg, cuda)}
+    gamma = 1e-3
+    b = torch.from_numpy(inp["router_bias"].copy()).to(cuda)
+    moe.moe_router_bias_update(cfg, g["ws"], b, gamma)
+    got = b.cpu().numpy()
+    if w.n_tokens == 0:
+        assert np.array_equal(got, inp["router_bias"])
+        return
+    r = oracle.route(inp["x"], inp["w_router"], inp["router_bias"], w.top_k, w.bias_mode)
+    # the device's own picks (equal to the oracle's unless a near-tie flipped)
+    picks = np.rint(g["freq"].astype(np.float64) * w.n_tokens * w.top_k).astype(np.int64)
+    if np.array_equal(g["idx"], r["idx"]):
+        assert np.array_equal(picks, r["picks"])
+    expect = oracle.router_bias_update(inp["router_bias"], picks, w.n_tokens, w.top_k, gamma)
+    assert np.array_equal(got, expect)
+
+
+def test_bias_update_rejects_bad_args(cuda):
+    w = synth.small_workload("dsv2_select", n_tokens=64, d_model=64, n_experts=16, top_k=2)
+    cfg = config_of(w)
+    ws = moe.alloc_workspace(cfg, cuda)
+    b = torch.zeros(16, device=cuda)
+    with pytest.raises(moe.MoeError):
+        moe.moe_router_bias_update(cfg, ws, b, float("nan"))
+    bad = config_of(w)
+    bad.bias_mode = 7
+    with pytest.raises(moe.MoeError):
+        moe.moe_router_bias_update(bad, ws, b, 1e-3)
