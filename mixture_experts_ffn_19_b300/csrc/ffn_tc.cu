@@ -281,29 +281,46 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ 
 namespace swp {
 
 constexpr int BM = 128, TOK = 64, BK = 64;
+constexpr int TOKB = 16;                       // token rows per TMA box
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = TOK * BK * 2;
+constexpr int BQ_BYTES = TOKB * BK * 2;        // one 16-row token box
 constexpr int A8_BYTES = BM * BK;              // E4M3 weight tile (W8 staging)
 constexpr int TMEM_COLS = 128;                 // two 64-column accumulators
 constexpr int XS = TOK + 1;                    // exchange row (floats), conflict-free
-constexpr int MAX_STAGES = 8;
-
-#ifndef MOE_FP8_CONV_WARPS
-#define MOE_FP8_CONV_WARPS 4
+constexpr int MAX_STAGES = 10;
+#ifndef MOE_FP8_CONV_GROUPS
+#define MOE_FP8_CONV_GROUPS 1
 #endif
-constexpr int CONV_WARPS = MOE_FP8_CONV_WARPS;     // converter warps (W8), from warp 6
+#ifndef MOE_FP8_TOK
+#define MOE_FP8_TOK 64
+#endif
+#ifndef MOE_FP8_STAGES
+#define MOE_FP8_STAGES 4
+#endif
+constexpr int CONV_WARPS = 4;                  // converter warps per group (W8)
+constexpr int CONV_GROUPS = MOE_FP8_CONV_GROUPS;  // groups take alternate stages
 
+// bf16 weights: one ring of [A (bf16 weights) | B (tokens)] stages, 64 deep
+// in K.  E4M3 weights: stages 128 deep in K, so every weight row is read as
+// a whole 128-byte line (64-byte pieces of rows 8 KB apart held the DRAM
+// below half its bandwidth): a TMA ring of [B (2 K-chunks) | E4M3 tile]
+// stages and a ring of converted stages of two bf16 A tiles.
 template <bool W8>
 struct Shape {
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + (W8 ? A8_BYTES : 0);
-  static constexpr int STAGES = W8 ? 6 : 8;
-  static constexpr int THREADS = W8 ? 192 + 32 * CONV_WARPS : 192;
+  static constexpr int KSUB = W8 ? 2 : 1;               // 64-deep K-chunks per stage
+  static constexpr int TOK = W8 ? MOE_FP8_TOK : swp::TOK;   // tokens per chunk
+  static constexpr int B_BYTES = TOK * BK * 2;
+  static constexpr int STAGE_BYTES = W8 ? KSUB * (B_BYTES + A8_BYTES) : A_BYTES + B_BYTES;
+  static constexpr int STAGES = W8 ? MOE_FP8_STAGES : 8;    // TMA ring
+  static constexpr int A_STAGES = W8 ? 2 : 0;           // converted ring (KSUB A tiles each)
+  static constexpr int THREADS = W8 ? 192 + 32 * CONV_WARPS * CONV_GROUPS : 192;
 };
 
 struct Ctrl {
   uint64_t full[MAX_STAGES];
   uint64_t empty[MAX_STAGES];
-  uint64_t conv[MAX_STAGES];     // W8: bf16 weight tile written
+  uint64_t conv[4];              // W8: converted bf16 tile ready
+  uint64_t afree[4];             // W8: converted tile consumed by the MMA
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t xfull;                // up values written to the exchange buffer
@@ -317,10 +334,16 @@ struct Ctrl {
 
 constexpr size_t XCH_BYTES = (size_t)64 * XS * 4;
 template <bool W8>
+constexpr size_t ring_bytes() {
+  return (size_t)Shape<W8>::STAGES * Shape<W8>::STAGE_BYTES +
+         (size_t)Shape<W8>::A_STAGES * Shape<W8>::KSUB * A_BYTES;
+}
+template <bool W8>
 constexpr size_t smem_bytes() {
-  return 1024 + (size_t)Shape<W8>::STAGES * Shape<W8>::STAGE_BYTES + XCH_BYTES + sizeof(Ctrl);
+  return 1024 + ring_bytes<W8>() + XCH_BYTES + sizeof(Ctrl);
 }
 static_assert(smem_bytes<true>() <= 232448 && smem_bytes<false>() <= 232448, "shared memory");
+static_assert(Shape<true>::A_STAGES % CONV_GROUPS == 0, "a converted slot belongs to one group");
 
 struct Params {
   int E, S, N, K, n_out, n_fb;   // n_fb: feature blocks per segment
@@ -361,19 +384,35 @@ ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_consta
   // tmB0/tmB1: token rows (x_perm / x for GEMM-1, H for GEMM-2);
   // tmA0/tmA1: weights (gate / up for GEMM-1, down for GEMM-2), bf16 or E4M3
   constexpr int STAGES = Shape<W8>::STAGES, STAGE_BYTES = Shape<W8>::STAGE_BYTES;
+  constexpr int A_STAGES = Shape<W8>::A_STAGES, KSUB = Shape<W8>::KSUB;
+  constexpr int TOK = Shape<W8>::TOK, B_BYTES = Shape<W8>::B_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  float* xch = reinterpret_cast<float*>(smem + (size_t)STAGES * STAGE_BYTES);
-  Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + (size_t)STAGES * STAGE_BYTES + XCH_BYTES);
+  float* xch = reinterpret_cast<float*>(smem + ring_bytes<W8>());
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + ring_bytes<W8>() + XCH_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nseg = p.E + p.S;
+  // tiles of TMA stage s1 and converted stage s2, K-chunk j (all 1024-byte
+  // aligned): W8 stage = [B0 | B1 | E4M3 128 rows x 128 bytes], converted
+  // stage = [A0 | A1]
+  auto b_tile = [&](int s1, int j) {
+    return smem + (size_t)s1 * STAGE_BYTES + (W8 ? j * B_BYTES : A_BYTES);
+  };
+  auto w8_tile = [&](int s1) { return smem + (size_t)s1 * STAGE_BYTES + KSUB * B_BYTES; };
+  auto a_tile = [&](int s1, int s2, int j) {
+    return W8 ? smem + (size_t)STAGES * STAGE_BYTES + ((size_t)s2 * KSUB + j) * A_BYTES
+              : smem + (size_t)s1 * STAGE_BYTES;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&ctrl->full[s], 1);
       mbar_init(&ctrl->empty[s], 1);
+    }
+    for (int s = 0; s < A_STAGES; ++s) {
       mbar_init(&ctrl->conv[s], 32 * CONV_WARPS);
+      mbar_init(&ctrl->afree[s], 1);
     }
     for (int b = 0; b < 2; ++b) { mbar_init(&ctrl->tfull[b], 1); mbar_init(&ctrl->tempty[b], 128); }
     mbar_init(&ctrl->xfull, 64);
@@ -398,7 +437,7 @@ ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_consta
   tc_fence_after();
   const uint32_t tmem_base = ctrl->tmem_base;
   const int total_tiles = ctrl->total_chunks * p.n_fb;
-  const int KB = (p.K + BK - 1) / BK;
+  const int KB = (p.K + BK * KSUB - 1) / (BK * KSUB);   // stages per tile
   volatile int* abort = &ctrl->abort;
   const Ctrl* cc = ctrl;
   // tile -> (segment, feature block, token chunk); chunk fastest
@@ -424,22 +463,29 @@ ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_consta
         int b_row = p.offsets[seg] + ch * TOK;
         if (MODE == 0 && seg >= p.E) { bmap = &tmB1; b_row = ch * TOK; }
         const int a_row = seg * p.n_out + fb * (MODE == 0 ? BM / 2 : BM);
+        // only the 16-row token boxes this chunk uses (decode experts see a few tokens)
+        const int nq = (min(TOK, seg_rows(p, seg) - ch * TOK) + TOKB - 1) / TOKB;
         for (int kb = 0; kb < KB; ++kb, ++kc) {
           const int st = kc % STAGES;
           const uint32_t ph = (kc / STAGES) & 1;
           if (!mbar_wait(&ctrl->empty[st], ph ^ 1, abort, p.status)) break;
-          uint8_t* a_s = smem + (size_t)st * STAGE_BYTES;
-          // W8: the E4M3 weight tile goes to the staging buffer after B
-          uint8_t* w_s = W8 ? a_s + A_BYTES + B_BYTES : a_s;
-          const int half = W8 ? A8_BYTES / 2 : A_BYTES / 2;
-          mbar_arrive_expect_tx(&ctrl->full[st], W8 ? A8_BYTES + B_BYTES : STAGE_BYTES);
+          // weights: the bf16 A tile, or the E4M3 tile the converters widen
+          uint8_t* w_s = W8 ? w8_tile(st) : a_tile(st, 0, 0);
+          const int half = W8 ? KSUB * A8_BYTES / 2 : A_BYTES / 2;
+          const int k0 = kb * BK * KSUB;
+          mbar_arrive_expect_tx(&ctrl->full[st],
+                                KSUB * ((W8 ? A8_BYTES : A_BYTES) + nq * BQ_BYTES));
           if (MODE == 0) {
-            tma_load_2d(w_s, &tmA0, &ctrl->full[st], kb * BK, a_row);
-            tma_load_2d(w_s + half, &tmA1, &ctrl->full[st], kb * BK, a_row);
+            tma_load_2d(w_s, &tmA0, &ctrl->full[st], k0, a_row);
+            tma_load_2d(w_s + half, &tmA1, &ctrl->full[st], k0, a_row);
           } else {
-            tma_load_2d(w_s, &tmA0, &ctrl->full[st], kb * BK, a_row);
+            tma_load_2d(w_s, &tmA0, &ctrl->full[st], k0, a_row);
           }
-          tma_load_2d(a_s + A_BYTES, bmap, &ctrl->full[st], kb * BK, b_row);
+#pragma unroll
+          for (int j = 0; j < KSUB; ++j)
+            for (int q = 0; q < nq; ++q)
+              tma_load_2d(b_tile(st, j) + q * BQ_BYTES, bmap, &ctrl->full[st], k0 + j * BK,
+                          b_row + q * TOKB);
         }
       }
     }
@@ -459,50 +505,72 @@ ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_consta
         for (int kb = 0; kb < KB; ++kb, ++kc) {
           const int st = kc % STAGES;
           const uint32_t ph = (kc / STAGES) & 1;
-          if (!mbar_wait(W8 ? &ctrl->conv[st] : &ctrl->full[st], ph, abort, p.status)) { ok = false; break; }
+          constexpr int AS = A_STAGES > 0 ? A_STAGES : 1;
+          const int s2 = W8 ? (int)(kc % AS) : 0;
+          const uint32_t ph2 = W8 ? (kc / AS) & 1 : 0;
+          // W8: the converted tile (its converters saw this stage's TMA land)
+          if (!mbar_wait(W8 ? &ctrl->conv[s2] : &ctrl->full[st], W8 ? ph2 : ph, abort, p.status)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + (size_t)st * STAGE_BYTES);
-          const uint64_t adesc = sdesc_kmajor_sw128(a_addr);
-          const uint64_t bdesc = sdesc_kmajor_sw128(a_addr + A_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            umma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+          for (int j = 0; j < KSUB; ++j) {
+            const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(a_tile(st, s2, j)));
+            const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(b_tile(st, j)));
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+              umma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | j | k) != 0);
+          }
           umma_commit(&ctrl->empty[st]);
+          if (W8) umma_commit(&ctrl->afree[s2]);
         }
         if (!ok) break;
         umma_commit(&ctrl->tfull[buf]);
       }
     }
-  } else if (W8 && warp >= 6 && warp < 6 + CONV_WARPS) {
-    // converter warps: E4M3 staging tile -> bf16 tile in the 128-byte swizzled
-    // K-major layout (16-byte chunk c of row r at chunk c ^ (r & 7)); 8 threads
-    // per row, 4 * CONV_WARPS rows per pass
-    constexpr int ROWS_PER_PASS = 4 * CONV_WARPS;
-    const int ct = threadIdx.x - 192;
+  } else if (W8 && warp >= 6 && warp < 6 + CONV_WARPS * CONV_GROUPS) {
+    // converter warps: E4M3 staging tile (128 rows x 128 codes) -> two bf16
+    // tiles in the 128-byte swizzled K-major layout (16-byte chunk c of row r
+    // at chunk c ^ (r & 7)); 16 threads per row, 2 * CONV_WARPS rows per pass
+    constexpr int ROWS_PER_PASS = 2 * CONV_WARPS;
+    const int grp = (threadIdx.x - 192) / (32 * CONV_WARPS);   // this group's stages: kc % CONV_GROUPS
+    const int ct = (threadIdx.x - 192) % (32 * CONV_WARPS);
     uint32_t kc = 0;
     for (int T = blockIdx.x; T < total_tiles && !*abort; T += gridDim.x) {
       bool ok = true;
       for (int kb = 0; kb < KB; ++kb, ++kc) {
+        if ((int)(kc % CONV_GROUPS) != grp) continue;
         const int st = kc % STAGES;
         const uint32_t ph = (kc / STAGES) & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&ctrl->full[st], ph, abort, p.status))) { ok = false; break; }
-        uint8_t* a_s = smem + (size_t)st * STAGE_BYTES;
-        const uint8_t* w_s = a_s + A_BYTES + B_BYTES;
-        // all of this thread's codes first (their loads in flight together),
-        // then the conversions and swizzled stores
+        constexpr int AS = A_STAGES > 0 ? A_STAGES : 1;   // (bf16 weights: no converter)
+        const int s2 = kc % AS;
+        const uint32_t ph2 = (kc / AS) & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&ctrl->full[st], ph, abort, p.status) &&
+                                         mbar_wait(&ctrl->afree[s2], ph2 ^ 1, abort, p.status))) {
+          ok = false;
+          break;
+        }
+        const uint8_t* w_s = w8_tile(st);
+        // 8 codes per thread and pass: chunk c16 of the row's 16, i.e. K-chunk
+        // j = c16 / 8, 16-byte chunk c = c16 % 8 of the bf16 row.  All of this
+        // thread's codes first (loads in flight together), then conversions
+        // and swizzled stores.
         constexpr int PASSES = BM / ROWS_PER_PASS;
-        const int c = ct & 7;
+        const int c16 = ct & 15, j = c16 >> 3, c = c16 & 7;
+        uint8_t* a_s = a_tile(st, s2, j);
         uint2 v[PASSES];
 #pragma unroll
         for (int pass = 0; pass < PASSES; ++pass)
-          v[pass] = *reinterpret_cast<const uint2*>(w_s + (pass * ROWS_PER_PASS + (ct >> 3)) * BK + c * 8);
+          v[pass] = *reinterpret_cast<const uint2*>(w_s + (pass * ROWS_PER_PASS + (ct >> 4)) * (BK * KSUB) +
+                                                    c16 * 8);
 #pragma unroll
         for (int pass = 0; pass < PASSES; ++pass) {
-          const int r = pass * ROWS_PER_PASS + (ct >> 3);
+          const int r = pass * ROWS_PER_PASS + (ct >> 4);
           *reinterpret_cast<uint4*>(a_s + r * 128 + ((c ^ (r & 7)) << 4)) = e4m3x8_to_bf16x8(v[pass]);
         }
         fence_proxy_async_smem();
-        mbar_arrive(&ctrl->conv[st]);
+        mbar_arrive(&ctrl->conv[s2]);
       }
       if (!ok) break;
     }
@@ -624,12 +692,13 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D E4M3 map over a row-major [rows, cols] byte matrix, box [box_rows, 64],
-// no swizzle (the converter warps lay the bf16 tile out themselves).
+// 2-D E4M3 map over a row-major [rows, cols] byte matrix, box [box_rows, 128]
+// (whole 128-byte lines), no swizzle (the converter warps lay the bf16 tiles
+// out themselves).
 bool make_map8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols};
-  const cuuint32_t box[2] = {BK, box_rows};
+  const cuuint32_t box[2] = {2 * BK, box_rows};
   const cuuint32_t elem[2] = {1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
                   box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -666,8 +735,8 @@ cudaError_t launch_swap(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) {
     return W8 ? make_map8(m, base, rows, cols, box) : make_map(m, base, rows, cols, box);
   };
   CUtensorMap b0, b1, a0, a1;
-  if (!make_map(&b0, p.x_perm, (uint64_t)p.max_rows, p.d, swp::TOK) ||
-      !make_map(&b1, p.x, (uint64_t)p.N, p.d, swp::TOK) ||
+  if (!make_map(&b0, p.x_perm, (uint64_t)p.max_rows, p.d, swp::TOKB) ||
+      !make_map(&b1, p.x, (uint64_t)p.N, p.d, swp::TOKB) ||
       !wmap(&a0, p.w_gate, (uint64_t)ET * p.F, p.d, swp::BM / 2) ||
       !wmap(&a1, p.w_up, (uint64_t)ET * p.F, p.d, swp::BM / 2))
     return cudaErrorInvalidValue;
@@ -678,7 +747,7 @@ cudaError_t launch_swap(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) {
   count_launch();
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   if (mid) cudaEventRecord(mid, s);
-  if (!make_map(&b0, p.h, (uint64_t)p.max_total_rows, p.F, swp::TOK) ||
+  if (!make_map(&b0, p.h, (uint64_t)p.max_total_rows, p.F, swp::TOKB) ||
       !wmap(&a0, p.w_down, (uint64_t)ET * p.d, p.F, swp::BM))
     return cudaErrorInvalidValue;
   swp::Params t2{p.E, p.S, p.N, p.F, p.d, (p.d + swp::BM - 1) / swp::BM, p.offsets, p.counts,
