@@ -216,9 +216,12 @@ def measured_traffic(kernel: str, workload: str):
         return None
 
 
+_GEMM_SOURCES = ["mixture_experts_ffn_19_b300/csrc/ffn_tc.cu",
+                 "mixture_experts_ffn_19_b300/csrc/common.cuh"]
 TRAFFIC_SOURCES = {
-    "ffn_tc_kernel<0>": ["mixture_experts_ffn_19_b300/csrc/ffn_tc.cu",
-                         "mixture_experts_ffn_19_b300/csrc/common.cuh"],
+    "ffn_tc_kernel<0>": _GEMM_SOURCES,
+    "ffn_tc_swap_kernel<0>": _GEMM_SOURCES,
+    "ffn_tc_swap_kernel<0,fp8>": _GEMM_SOURCES,
 }
 
 

@@ -350,9 +350,10 @@ RouteSplit route_split(int N, int d, bool bf16) {
   const int tile = bf16 ? 128 : kTM;
   const int tiles = N > 0 ? (N + tile - 1) / tile : 1;
   const int kblocks = (d + 63) / 64;
-  // about one CTA per SM, at most 16 slices (each slice is one more partial
-  // per logit to read back)
-  int ks = (148 + tiles - 1) / tiles;
+  // at most one CTA per SM (the tensor-core router holds an SM's TMEM), so
+  // one wave: a second, partial wave would double the time; at most 16
+  // slices (each slice is one more partial per logit to read back)
+  int ks = 148 / tiles;
   ks = ks < 1 ? 1 : (ks > 16 ? 16 : ks);
   ks = ks > kblocks ? kblocks : ks;
   const int k_slice = (kblocks + ks - 1) / ks * 64;
