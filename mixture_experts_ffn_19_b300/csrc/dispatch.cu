@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchPa
   constexpr int TE = 64;                         // experts per staged probability tile
   __shared__ uint32_t bits[kMaxExperts * kRrWords];
   __shared__ float prob_s[kRrThreads][TE + 1];
-  __shared__ unsigned char full_s[kMaxExperts];
+  __shared__ unsigned long long full_m[kMaxExperts / 64];   // bit e: expert e was full at round start
   __shared__ int fill_s[kMaxExperts];
   const int tid = threadIdx.x;
   const int nch = (N + kRrThreads - 1) / kRrThreads;
@@ -223,22 +223,30 @@ __global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchPa
   for (int round = 0;; ++round) {
     if (round >= kMaxRounds || round > E + 1) { set_status(p.status, kDevBadState); break; }
     // ---- phase A: proposals, per-chunk bitmap ranks and counts
-    for (int e = tid; e < E; e += kRrThreads) full_s[e] = __ldcg(&rr->fill[cur][e]) >= C;
+    for (int w = tid; w < kMaxExperts / 64; w += kRrThreads) full_m[w] = 0ull;
+    __syncthreads();
+    for (int e = tid; e < E; e += kRrThreads)
+      if (__ldcg(&rr->fill[cur][e]) >= C) atomicOr(&full_m[e >> 6], 1ull << (e & 63));
     __syncthreads();
     for (int c = blockIdx.x; c < nch; c += gridDim.x) {
       for (int i = tid; i < E * kRrWords; i += kRrThreads) bits[i] = 0;
       const int t = c * kRrThreads + tid;
+      // held / prop stay in registers: every index below is a compile-time
+      // constant after unrolling (slots past k are guarded)
       int held[kMaxTopk], prop[kMaxTopk];
       bool mine = false;
-      for (int j = 0; j < k; ++j) {
-        held[j] = t < N ? p.final_idx[(size_t)t * k + j] : -1;
+#pragma unroll
+      for (int j = 0; j < kMaxTopk; ++j) {
+        held[j] = (j < k && t < N) ? p.final_idx[(size_t)t * k + j] : -1;
         prop[j] = -1;
         mine |= held[j] == kPendingMark;
       }
       bool any = false;
       bool tile_valid = false;                   // E <= TE: one staged tile serves every slot
       if (__syncthreads_or(mine)) {
-        for (int j = 0; j < k; ++j) {
+#pragma unroll
+        for (int j = 0; j < kMaxTopk; ++j) {
+          if (j >= k) break;
           const bool need = held[j] == kPendingMark;
           if (!__syncthreads_or(need)) continue;
           float bp = -1.f;
@@ -267,13 +275,20 @@ __global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchPa
               __syncthreads();
             }
             if (need) {
-              for (int col = 0; col < TE && e0 + col < E; ++col) {
-                const int e = e0 + col;
-                if (full_s[e]) continue;
-                bool skip = false;
-                for (int jj = 0; jj < k; ++jj) skip |= (held[jj] == e) | (jj < j && prop[jj] == e);
-                if (skip) continue;
+              // experts of this tile the slot may not take: full at the start of
+              // the round, held by the token, or proposed by an earlier slot
+              uint64_t excl = full_m[e0 >> 6];
+#pragma unroll
+              for (int jj = 0; jj < kMaxTopk; ++jj) {
+                const int eh = held[jj] - e0, ep = prop[jj] - e0;
+                if (jj < k && eh >= 0 && eh < TE) excl |= 1ull << eh;
+                if (jj < j && ep >= 0 && ep < TE) excl |= 1ull << ep;
+              }
+              const int ncol = min(TE, E - e0);
+              for (int col = 0; col < ncol; ++col) {
+                if ((excl >> col) & 1ull) continue;
                 const float pe = prob_s[tid][col];
+                const int e = e0 + col;
                 if (be < 0 || better(pe, e, bp, be)) { bp = pe; be = e; }
               }
             }
@@ -291,7 +306,9 @@ __global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchPa
       }
       __syncthreads();
       if (mine) {
-        for (int j = 0; j < k; ++j) {
+#pragma unroll
+        for (int j = 0; j < kMaxTopk; ++j) {
+          if (j >= k) break;
           const int e = prop[j];
           int r = -1;
           if (e >= 0) {
