@@ -149,10 +149,17 @@ __global__ void __launch_bounds__(kThreads) route_finish_kernel(RouteParams p, R
     if (t >= N) break;
     float v[EJ], raw[EJ];
     float m = -INFINITY, mr = -INFINITY;
+    // logits: the K-slice partials summed in slice order (compensated fp32)
 #pragma unroll
     for (int c = 0; c < EJ; ++c) {
       const int e = lane + 32 * c;
-      raw[c] = (e < E) ? p.part[(size_t)t * E + e] : -INFINITY;
+      if (e < E) {
+        KahanF z;
+        for (int s0 = 0; s0 < sp.ks; ++s0) z.add(p.part[((size_t)s0 * N + t) * E + e]);
+        raw[c] = z.s;
+      } else {
+        raw[c] = -INFINITY;
+      }
       v[c] = (e < E) ? raw[c] + (bias_logit ? b[c] : 0.f) : -INFINITY;
       m = fmaxf(m, v[c]);
       mr = fmaxf(mr, raw[c]);
@@ -285,24 +292,6 @@ __global__ void bias_update_kernel(const int* picks, float* bias, int N, int E, 
   else if (load < mean) bias[e] = bias[e] + gamma;
 }
 
-// Logits from the K-slice partials: part[0][t][e] = sum_s part[s][t][e], a
-// compensated fp32 sum in slice order (8 independent loads in flight).
-__global__ void __launch_bounds__(kThreads) route_reduce_kernel(float* part, int ks, size_t n) {
-  const size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x;
-  if (i >= n) return;
-  KahanF z;
-  int s = 0;
-  for (; s + 8 <= ks; s += 8) {
-    float v[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = part[(size_t)(s + u) * n + i];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) z.add(v[u]);
-  }
-  for (; s < ks; ++s) z.add(part[(size_t)s * n + i]);
-  part[i] = z.s;
-}
-
 template <int EJ>
 cudaError_t launch_simt_t(const RouteParams& p, const RouteSplit& sp, cudaStream_t s) {
   const size_t smem = sizeof(float) * ((size_t)kTM * kXS + (size_t)EJ * 32 * kXS);
@@ -379,12 +368,6 @@ cudaError_t launch_route(const RouteParams& p, bool bf16, cudaStream_t s) {
     err = [&]() -> cudaError_t { MOE_EJ_SWITCH(p.E, launch_simt_t, p, sp, s) }();
   }
   if (err != cudaSuccess) return err;
-  if (sp.ks > 1) {
-    const size_t n = (size_t)p.N * p.E;
-    route_reduce_kernel<<<(unsigned)((n + kThreads - 1) / kThreads), kThreads, 0, s>>>(p.part, sp.ks, n);
-    count_launch();
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  }
   MOE_EJ_SWITCH(p.E, launch_finish_t, p, sp, s)
 }
 
