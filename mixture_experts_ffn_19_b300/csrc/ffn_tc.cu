@@ -288,17 +288,7 @@ constexpr int A8_BYTES = BM * BK;              // E4M3 weight tile (W8 staging)
 constexpr int TMEM_COLS = 128;                 // two 64-column accumulators
 constexpr int XS = TOK + 1;                    // exchange row (floats), conflict-free
 constexpr int MAX_STAGES = 10;
-#ifndef MOE_FP8_CONV_GROUPS
-#define MOE_FP8_CONV_GROUPS 1
-#endif
-#ifndef MOE_FP8_TOK
-#define MOE_FP8_TOK 64
-#endif
-#ifndef MOE_FP8_STAGES
-#define MOE_FP8_STAGES 4
-#endif
-constexpr int CONV_WARPS = 4;                  // converter warps per group (W8)
-constexpr int CONV_GROUPS = MOE_FP8_CONV_GROUPS;  // groups take alternate stages
+constexpr int CONV_WARPS = 4;                  // W8 converter warps 6..9
 
 // bf16 weights: one ring of [A (bf16 weights) | B (tokens)] stages, 64 deep
 // in K.  E4M3 weights: stages 128 deep in K, so every weight row is read as
@@ -308,12 +298,12 @@ constexpr int CONV_GROUPS = MOE_FP8_CONV_GROUPS;  // groups take alternate stage
 template <bool W8>
 struct Shape {
   static constexpr int KSUB = W8 ? 2 : 1;               // 64-deep K-chunks per stage
-  static constexpr int TOK = W8 ? MOE_FP8_TOK : swp::TOK;   // tokens per chunk
+  static constexpr int TOK = swp::TOK;                   // tokens per chunk
   static constexpr int B_BYTES = TOK * BK * 2;
   static constexpr int STAGE_BYTES = W8 ? KSUB * (B_BYTES + A8_BYTES) : A_BYTES + B_BYTES;
-  static constexpr int STAGES = W8 ? MOE_FP8_STAGES : 8;    // TMA ring
+  static constexpr int STAGES = W8 ? 4 : 8;             // TMA ring
   static constexpr int A_STAGES = W8 ? 2 : 0;           // converted ring (KSUB A tiles each)
-  static constexpr int THREADS = W8 ? 192 + 32 * CONV_WARPS * CONV_GROUPS : 192;
+  static constexpr int THREADS = W8 ? 192 + 32 * CONV_WARPS : 192;
 };
 
 struct Ctrl {
@@ -343,7 +333,6 @@ constexpr size_t smem_bytes() {
   return 1024 + ring_bytes<W8>() + XCH_BYTES + sizeof(Ctrl);
 }
 static_assert(smem_bytes<true>() <= 232448 && smem_bytes<false>() <= 232448, "shared memory");
-static_assert(Shape<true>::A_STAGES % CONV_GROUPS == 0, "a converted slot belongs to one group");
 
 struct Params {
   int E, S, N, K, n_out, n_fb;   // n_fb: feature blocks per segment
@@ -529,18 +518,16 @@ ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_consta
         umma_commit(&ctrl->tfull[buf]);
       }
     }
-  } else if (W8 && warp >= 6 && warp < 6 + CONV_WARPS * CONV_GROUPS) {
+  } else if (W8 && warp >= 6 && warp < 6 + CONV_WARPS) {
     // converter warps: E4M3 staging tile (128 rows x 128 codes) -> two bf16
     // tiles in the 128-byte swizzled K-major layout (16-byte chunk c of row r
     // at chunk c ^ (r & 7)); 16 threads per row, 2 * CONV_WARPS rows per pass
     constexpr int ROWS_PER_PASS = 2 * CONV_WARPS;
-    const int grp = (threadIdx.x - 192) / (32 * CONV_WARPS);   // this group's stages: kc % CONV_GROUPS
-    const int ct = (threadIdx.x - 192) % (32 * CONV_WARPS);
+    const int ct = threadIdx.x - 192;
     uint32_t kc = 0;
     for (int T = blockIdx.x; T < total_tiles && !*abort; T += gridDim.x) {
       bool ok = true;
       for (int kb = 0; kb < KB; ++kb, ++kc) {
-        if ((int)(kc % CONV_GROUPS) != grp) continue;
         const int st = kc % STAGES;
         const uint32_t ph = (kc / STAGES) & 1;
         constexpr int AS = A_STAGES > 0 ? A_STAGES : 1;   // (bf16 weights: no converter)
