@@ -308,6 +308,16 @@ int moe_dispatch_noalloc(const moe_config* cfg, const int32_t* topk_idx, const f
                          int32_t* perm, void* x_perm, const moe_stats* stats,
                          int32_t* device_status, void* stream);
 
+/* Failure-path self-test (no page has a counterpart: it exercises this
+ * library's error handling).  Launches one kernel on `stream` whose bounded
+ * wait on an mbarrier that nothing arrives on runs out after limit_us
+ * microseconds (1 .. 1,000,000); like a stalled pipeline it records
+ * MOE_ERR_TIMEOUT in the workspace status word (read it with
+ * moe_device_status) and returns, leaving the context usable.  No fault,
+ * trap or unbounded wait is involved.  The status word is the first 4 bytes
+ * of any workspace, so any workspace of at least 4 bytes serves. */
+int moe_selftest_timeout(void* workspace, size_t workspace_bytes, uint32_t limit_us, void* stream);
+
 /* Synchronises `stream`, then copies the workspace's device status word to
  * *status_out (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE) and clears it. */
 int moe_device_status(void* workspace, void* stream, int32_t* status_out);

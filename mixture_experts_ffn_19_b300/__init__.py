@@ -92,6 +92,7 @@ _SIGS = {
     "moe_forward_fp8": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P,
                                        ctypes.POINTER(moe_stats), _P, ctypes.c_size_t, _P,
                                        ctypes.POINTER(moe_timing)]),
+    "moe_selftest_timeout": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_uint32, _P]),
     "moe_device_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "moe_kernel_launches": (ctypes.c_int64, []),
 }
@@ -252,6 +253,12 @@ def moe_forward_fp8(cfg, x, w_router, router_bias, w_gate, w_up, w_down, scales,
         ctypes.byref(stats) if stats is not None else None,
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream),
         ctypes.byref(timing) if timing is not None else None))
+
+
+def moe_selftest_timeout(workspace, limit_us, stream=None) -> int:
+    return _check("moe_selftest_timeout", lib().moe_selftest_timeout(
+        _ptr(workspace), workspace.numel() * workspace.element_size(), int(limit_us),
+        _stream(stream)))
 
 
 def moe_device_status(workspace, stream=None) -> int:

@@ -437,6 +437,15 @@ int moe_forward_fp8(const moe_config* c, const void* x, const void* w_router, co
                       stats, ws, ws_bytes, stream, timing);
 }
 
+int moe_selftest_timeout(void* ws, size_t ws_bytes, uint32_t limit_us, void* stream) {
+  if (!ws || !aligned16(ws) || ws_bytes < sizeof(int32_t)) return MOE_ERR_INVALID_ARG;
+  if (limit_us < 1 || limit_us > 1000000) return MOE_ERR_INVALID_ARG;
+  return launch_wait_selftest(static_cast<int*>(ws), (uint64_t)limit_us * 1000ull,
+                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
 int moe_device_status(void* ws, void* stream, int32_t* status_out) {
   if (!ws || !status_out) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

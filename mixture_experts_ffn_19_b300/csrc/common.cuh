@@ -121,17 +121,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with the given parity to complete, for at most
-// kWaitLimitNs.  On time-out, or when another role of the CTA has already
-// given up (*abort != 0), returns false; a time-out also records kDevTimeout.
+// limit_ns (kWaitLimitNs by default).  On time-out, or when another role of
+// the CTA has already given up (*abort != 0), returns false; a time-out also
+// records kDevTimeout.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          int* status) {
+                                          int* status, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 15u) == 0) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         *abort = 1;
         set_status(status, kDevTimeout);
         return false;

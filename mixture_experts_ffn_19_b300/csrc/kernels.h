@@ -42,6 +42,8 @@ struct RouteParams {
 cudaError_t launch_quantize_fp8(const void* w, int n_mat, int64_t per_mat, uint8_t* q, float* scales,
                                 int num_sms, cudaStream_t s);
 
+cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t s);
+
 cudaError_t launch_bias_update(const int* picks, float* bias, int N, int E, int k, float gamma,
                                cudaStream_t s);
 

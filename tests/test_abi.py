@@ -102,3 +102,8 @@ def test_zero_tokens_and_tiny_shapes_size_without_error(lib):
         assert moe.moe_workspace_size(c) > 0
     c = moe.make_config(0, 128, 8, 2, 256, act=moe.MOE_ACT_GELU, dtype=moe.MOE_F32, has_ffn_bias=True)
     assert moe.moe_workspace_size(c) > 0
+
+
+def test_selftest_rejects_missing_workspace(lib):
+    # host-side checks only: nothing is launched
+    assert lib.moe_selftest_timeout(None, 0, 1000, None) == moe.MOE_ERR_INVALID_ARG
