@@ -115,6 +115,28 @@ def test_forward_edge_cases(cuda):
         check_forward(w, inp, run_forward(w, inp, cuda, with_views=True))
 
 
+MAX_SIZES = [
+    # the largest E, k and S the header allows (256, 8, 8): 264 segments in the
+    # GEMM tile lists and 16 contributions per token in the combine.
+    # N*k > 64*E: 128-row tiles (prefill kernel), with reroute
+    synth.small_workload("e64_reroute", n_tokens=2500, d_model=64, n_experts=256, top_k=8,
+                         d_ff=64, n_shared=8, alpha=1.0),
+    # N*k <= 64*E and N <= 512: the weights-as-M kernel, capacity drop (C = 9)
+    synth.small_workload("dsv2", n_tokens=300, d_model=64, n_experts=256, top_k=8, d_ff=64,
+                         n_shared=8, cap_mode=synth.CAP_DROP, alpha=1.0),
+    # fp32 GELU experts with biases
+    synth.small_workload("tiny_fp32", n_tokens=300, d_model=64, n_experts=256, top_k=8,
+                         d_ff=64, n_shared=8),
+]
+
+
+@pytest.mark.parametrize("w", MAX_SIZES, ids=lambda w: w.name)
+def test_forward_max_sizes(cuda, w):
+    assert (w.n_experts, w.top_k, w.n_shared) == (256, 8, 8)   # MOE_MAX_EXPERTS/TOPK/SHARED
+    inp = synth.make_inputs(w)
+    check_forward(w, inp, run_forward(w, inp, cuda, with_views=True))
+
+
 def test_forward_zero_tokens(cuda):
     w = synth.small_workload("mixtral_prefill", n_tokens=0, d_model=64, d_ff=64)
     cfg = config_of(w)
