@@ -102,9 +102,12 @@ PINS = {
                     "<= half a step, zero matrix, hand case",
     "dequantize_fp8": "tests/test_oracle_fp8.py: product of the decoded code and the scale",
     "moe_forward": "tests/test_oracle_forward.py: E=1 dense layer, shared-only dense "
-                   "layer, token-permutation equivariance, linearity in the gates; "
-                   "no page prints a numeric layer output, so beyond these the "
-                   "whole-layer value is parity unpinned",
+                   "layer, k=E layer = probability-weighted dense mixture of every "
+                   "expert (logit and selection-only bias; a gate rotated to the "
+                   "wrong expert fails), token-permutation equivariance, linearity "
+                   "in the routed outputs, dropped slots contribute nothing; no page "
+                   "prints a numeric layer output, so the pins are these special "
+                   "cases and invariants",
 }
 
 

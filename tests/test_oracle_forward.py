@@ -90,3 +90,61 @@ def test_dropped_slot_contributes_nothing():
                 wts = {k: inp[k][e] for k in ("w_gate", "w_up", "w_down")}
                 y = y + float(out["w"][t, j]) * oracle.expert_ffn(oracle.widen(inp["x"][t:t + 1]), wts, 1)[0]
         np.testing.assert_allclose(out["y"][t], y if not np.isscalar(y) else np.zeros(32), atol=1e-12)
+
+
+
+def _dense_mixture(w, inp, bias_in_weights, roll=0):
+    """y = sum_e p_e(x) FFN_e(x) + shared FFN(x), every expert evaluated densely
+    with torch, p from scipy's softmax of the router logits (float64).  Returns y
+    and the elementwise bound sum_e |FFN_e(x)| that gate errors are scaled by.
+    roll != 0 pairs expert e with the gate of expert e + roll (a planted mistake)."""
+    from scipy.special import softmax
+    x = torch.tensor(oracle.widen(inp["x"]))
+    z = (x @ torch.tensor(oracle.widen(inp["w_router"])).T).numpy()
+    if bias_in_weights and inp["router_bias"] is not None:
+        z = z + np.asarray(inp["router_bias"], dtype=np.float64)
+    p = np.roll(softmax(z, axis=1), -roll, axis=1)
+    y = np.zeros((w.n_tokens, w.d_model))
+    scale = np.zeros_like(y)
+    for e in range(w.n_experts + w.n_shared):
+        wg, wu, wd = (torch.tensor(oracle.widen(inp[k][e])) for k in ("w_gate", "w_up", "w_down"))
+        f = (torch.nn.functional.silu(x @ wg.T) * (x @ wu.T) @ wd.T).numpy()
+        y += f * (p[:, e:e + 1] if e < w.n_experts else 1.0)
+        scale += np.abs(f)
+    return y, scale
+
+
+def _check_mixture(w, inp, bias_in_weights):
+    out = oracle.moe_forward(w, inp)
+    ref, scale = _dense_mixture(w, inp, bias_in_weights)
+    # the oracle's probabilities are float32 (the pages' fp32 softmax): a few
+    # ulps of each gate, times the expert outputs they scale
+    tol = 1e-6 * scale
+    assert np.all(np.abs(out["y"] - ref) <= tol)
+    wrong, _ = _dense_mixture(w, inp, bias_in_weights, roll=1)
+    assert np.mean(np.abs(out["y"] - wrong) > tol) > 0.9     # the pin tells them apart
+
+
+def test_all_experts_firing_is_the_probability_weighted_mixture():
+    # k = E and no capacity: every expert fires and the renormalised gates are
+    # the softmax probabilities themselves, distinct per expert, so a gate
+    # paired with the wrong expert's output (or a lost bias) changes y
+    w = _small("dsv2", n_tokens=25, d_model=32, n_experts=6, top_k=6, d_ff=40, n_shared=1,
+               cap_mode=synth.CAP_NONE)
+    inp = synth.make_inputs(w)
+    assert inp["router_bias"] is not None and np.ptp(inp["router_bias"]) > 0
+    _check_mixture(w, inp, bias_in_weights=True)
+
+
+def test_selection_bias_with_all_experts_firing_leaves_the_weights_unbiased():
+    # selection-only bias: with k = E the selection is everything, and the
+    # gates are the unbiased softmax probabilities
+    w = _small("dsv2_select", n_tokens=25, d_model=32, n_experts=6, top_k=6, d_ff=40,
+               n_shared=1, cap_mode=synth.CAP_NONE)
+    inp = synth.make_inputs(w)
+    assert w.bias_mode == 1 and np.ptp(inp["router_bias"]) > 0
+    _check_mixture(w, inp, bias_in_weights=False)
+    # and the biased softmax would not pass
+    out = oracle.moe_forward(w, inp)
+    biased, scale = _dense_mixture(w, inp, bias_in_weights=True)
+    assert np.mean(np.abs(out["y"] - biased) > 1e-6 * scale) > 0.9
