@@ -82,15 +82,18 @@ typedef enum { MOE_BIAS_LOGIT = 0, MOE_BIAS_SELECT = 1 } moe_bias_mode;
 #define MOE_MAX_TOPK 8           /* k <= min(E, 8)                        */
 #define MOE_MAX_SHARED 8         /* shared experts S                      */
 #define MOE_MAX_TOKENS (1 << 22) /* N                                     */
+#define MOE_MAX_DIM 65536        /* d and F: keeps the stacked weights'    *
+                                  * row coordinates, (E+S)*F and (E+S)*d,  *
+                                  * inside the int32 range of a TMA copy   */
 #define MOE_SEGMENT_ALIGN 128    /* rows; segment starts are multiples    */
 
 /* Layer shape and options (plain values, read on the host only). */
 typedef struct moe_config {
   int32_t n_tokens;        /* N >= 0 (N = 0 is a no-op)                    */
-  int32_t d_model;         /* d >= 1                                       */
+  int32_t d_model;         /* d, 8 .. MOE_MAX_DIM, a multiple of 8        */
   int32_t n_experts;       /* E routed experts, 1 .. MOE_MAX_EXPERTS       */
   int32_t top_k;           /* k, 1 .. min(E, MOE_MAX_TOPK)                 */
-  int32_t d_ff;            /* F, expert hidden width                       */
+  int32_t d_ff;            /* F, expert hidden width, like d               */
   int32_t n_shared;        /* S, 0 .. MOE_MAX_SHARED                       */
   int32_t act;             /* moe_act                                      */
   int32_t dtype;           /* moe_dtype                                    */

@@ -260,8 +260,8 @@ const char* moe_status_string(int st) {
 int moe_validate_config(const moe_config* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
   if (c->n_tokens < 0 || c->n_tokens > MOE_MAX_TOKENS) return MOE_ERR_INVALID_ARG;
-  if (c->d_model < 8 || c->d_model % 8 != 0) return MOE_ERR_INVALID_ARG;
-  if (c->d_ff < 8 || c->d_ff % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (c->d_model < 8 || c->d_model > MOE_MAX_DIM || c->d_model % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (c->d_ff < 8 || c->d_ff > MOE_MAX_DIM || c->d_ff % 8 != 0) return MOE_ERR_INVALID_ARG;
   if (c->n_experts < 1 || c->n_experts > MOE_MAX_EXPERTS) return MOE_ERR_INVALID_ARG;
   if (c->top_k < 1 || c->top_k > std::min(c->n_experts, MOE_MAX_TOPK)) return MOE_ERR_INVALID_ARG;
   if (c->n_shared < 0 || c->n_shared > MOE_MAX_SHARED) return MOE_ERR_INVALID_ARG;

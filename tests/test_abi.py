@@ -48,6 +48,11 @@ def test_validation(lib):
                              ("top_k", 0, moe.MOE_ERR_INVALID_ARG),
                              ("d_model", 4100, moe.MOE_ERR_INVALID_ARG),
                              ("d_ff", 12, moe.MOE_ERR_INVALID_ARG),
+                             # MOE_MAX_DIM = 65536 bounds d and F
+                             ("d_model", 65536 + 8, moe.MOE_ERR_INVALID_ARG),
+                             ("d_ff", 65536 + 8, moe.MOE_ERR_INVALID_ARG),
+                             ("d_model", 65536, moe.MOE_OK),
+                             ("d_ff", 65536, moe.MOE_OK),
                              ("n_tokens", -1, moe.MOE_ERR_INVALID_ARG),
                              ("cap_mode", 3, moe.MOE_ERR_INVALID_ARG),
                              ("alpha", 0.0, moe.MOE_ERR_INVALID_ARG),
