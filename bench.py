@@ -182,6 +182,18 @@ def layer_work(w, counts_kept, n_dropped):
             "total_flop": g1 + g2 + router}
 
 
+def gemm1_bytes(w, counts, rows: int) -> float:
+    """Algorithmic bytes of one gate/up GEMM launch: the gate (and up) weights of
+    every touched expert (routed experts with at least one kept row, plus the
+    shared ones), the launch's input rows and its output rows of H."""
+    es = 2 if w.dtype == synth.DT_BF16 else 4
+    wes = 1 if w.fp8_weights else es             # bytes per expert-weight element
+    touched = int((np.asarray(counts) > 0).sum()) + w.n_shared
+    nmat1 = 2 if w.act == synth.ACT_SWIGLU else 1
+    return float(touched * nmat1 * w.d_ff * w.d_model * wes + rows * w.d_model * es
+                 + rows * w.d_ff * es)
+
+
 def gemm1_kernel(w) -> str:
     """The gate/up GEMM kernel the library launches for this workload: the
     weights-as-M (swap-AB) kernel for E4M3 weights and for batches with at most
@@ -485,16 +497,12 @@ def bench_ours(args, w):
 
     pk = peaks()
     counts = st_t["counts"].cpu().numpy()
-    es = 2 if w.dtype == synth.DT_BF16 else 4
-    wes = 1 if w.fp8_weights else es             # bytes per expert-weight element
+    wes = 1 if w.fp8_weights else (2 if w.dtype == synth.DT_BF16 else 4)
     touched = int((counts > 0).sum()) + w.n_shared
     nmat1 = 2 if w.act == synth.ACT_SWIGLU else 1
-    rows = work["rows"]
-    # algorithmic bytes of the first expert GEMM: weights of touched experts, its
-    # input rows, its output rows
     g1_wbytes = touched * nmat1 * w.d_ff * w.d_model * wes
     g2_wbytes = touched * w.d_ff * w.d_model * wes
-    g1_bytes = g1_wbytes + rows * w.d_model * es + rows * w.d_ff * es
+    g1_bytes = gemm1_bytes(w, counts, work["rows"])
     g1_ms = statistics.mean(stage["gemm1"])
     g1_tflops = work["gemm1_flop"] / (g1_ms * 1e-3) / 1e12
     g1_gbs = g1_bytes / (g1_ms * 1e-3) / 1e9

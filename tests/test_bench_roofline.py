@@ -1,0 +1,51 @@
+"""The roofline numerator bench.py reports: algorithmic FLOPs and bytes of the
+gate/up GEMM, against values worked out by hand for the benchmark shapes, and
+the rule that names the kernel those figures belong to."""
+import numpy as np
+
+import bench
+import synth
+
+
+def test_mixtral_prefill_flops():
+    w = synth.WORKLOADS["mixtral_prefill"]
+    work = bench.layer_work(w, counts_kept=8192, n_dropped=0)
+    # every kept row: x (4096) against 2 x 14336 gate/up rows, 2 FLOP per MAC
+    assert work["gemm1_flop"] == 2 * 8192 * 4096 * 2 * 14336 == 1_924_145_348_608
+    assert work["gemm2_flop"] == work["gemm1_flop"] / 2
+    assert work["router_flop"] == 2 * 4096 * 4096 * 8
+    assert work["rows"] == 8192
+
+
+def test_shared_rows_count_once_per_token():
+    w = synth.WORKLOADS["dsv2"]                    # 2 shared experts
+    work = bench.layer_work(w, counts_kept=100, n_dropped=0)
+    assert work["rows"] == 100 + 2 * w.n_tokens
+
+
+def test_gemm1_bytes_decode_fp8():
+    w = synth.WORKLOADS["decode_mixtral_fp8"]      # 64 tokens, every expert touched
+    counts = np.full(8, 16)
+    got = bench.gemm1_bytes(w, counts, rows=128)
+    weights = 8 * 2 * 14336 * 4096                 # one byte per E4M3 code
+    assert got == weights + 128 * 4096 * 2 + 128 * 14336 * 2
+    # the recorded DRAM traffic of that launch is within 1 % of it
+    rec = bench.measured_traffic("ffn_tc_swap_kernel<0,fp8>", "decode_mixtral_fp8")
+    if rec is not None:
+        assert abs(rec / got - 1) < 0.01
+
+
+def test_gemm1_bytes_skip_untouched_experts():
+    w = synth.WORKLOADS["decode_dsv2"]             # bf16, 2 shared experts
+    counts = np.zeros(160, dtype=np.int64)
+    counts[[3, 7, 9]] = [1, 2, 5]
+    got = bench.gemm1_bytes(w, counts, rows=8 + 2 * 32)
+    assert got == (3 + 2) * 2 * 1536 * 5120 * 2 + 72 * 5120 * 2 + 72 * 1536 * 2
+
+
+def test_kernel_rule():
+    names = {n: bench.gemm1_kernel(w) for n, w in synth.WORKLOADS.items()}
+    assert names["mixtral_prefill"] == names["dsv2"] == names["e64_reroute"] == "ffn_tc_kernel<0>"
+    assert names["decode_mixtral"] == names["decode_dsv2"] == "ffn_tc_swap_kernel<0>"
+    assert names["decode_mixtral_fp8"] == names["decode_dsv2_fp8"] == "ffn_tc_swap_kernel<0,fp8>"
+    assert names["tiny_fp32"] == "ffn_simt_kernel<1>"
