@@ -1,10 +1,11 @@
-"""Plain float64 restatement of the MoE-FFN forward layer (test infrastructure only).
+"""Independent float64 NumPy restatement of the MoE-FFN forward layer (test
+infrastructure only).
 
-Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
-``bench.py`` may import this module.  Every step is written the way its page
-states it; library primitives (matmul, argsort, exp, erf) serve as steps, with
-no blocking, fusion or reordering.  Page keys [P1]..[P5] are defined in
-``oracle/__init__.py``.
+The oracle proper is the C++ library in this folder; this module restates the
+same steps a second way (library matmul, argsort, exp and erf as steps, no
+blocking, fusion or reordering) and serves only as one more pin of it
+(``tests/test_oracle_cross.py``).  No value the C++ oracle produces comes from
+here.  Page keys [P1]..[P5] are defined in ``oracle/__init__.py``.
 
 Inputs are the exact values the device receives (bf16 bit patterns or
 float32), widened exactly to float64.  Probabilities are computed in float64

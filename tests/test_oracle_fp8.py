@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import moe_oracle as O
+import oracle as O
 
 
 def torch_e4m3(v):

@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 from scipy.special import logsumexp
 
-from oracle import moe_oracle as O
+import oracle as O
 
 
 def test_z_loss_zero_logits_closed_form():
