@@ -321,6 +321,21 @@ int moe_dispatch_noalloc(const moe_config* cfg, const int32_t* topk_idx, const f
  * of any workspace, so any workspace of at least 4 bytes serves. */
 int moe_selftest_timeout(void* workspace, size_t workspace_bytes, uint32_t limit_us, void* stream);
 
+/* Grid-barrier failure-path self-test (no page has a counterpart: it exercises
+ * this library's error handling).  Launches one cooperative kernel of four
+ * CTAs on `stream`: CTA 0 never reaches the grid barrier -- the bounded
+ * barrier the cooperative reroute kernel uses -- while the other three run a
+ * chain of n_barriers (1 .. 4096) barriers.  Their first wait runs out after
+ * limit_us microseconds (1 .. 1,000,000): the first CTA to give up records
+ * MOE_ERR_TIMEOUT in the workspace status word and raises the barrier's abort
+ * flag, and every CTA then leaves at once, so the kernel ends after about one
+ * limit whatever n_barriers is.  The barrier state occupies workspace bytes
+ * 16..27 (zeroed by the call, stream-ordered), so the workspace must hold at
+ * least 28 bytes; it is overwritten.  No fault, trap or unbounded wait is
+ * involved; the context stays usable. */
+int moe_selftest_barrier_timeout(void* workspace, size_t workspace_bytes, uint32_t limit_us,
+                                 uint32_t n_barriers, void* stream);
+
 /* Synchronises `stream`, then copies the workspace's device status word to
  * *status_out (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE) and clears it. */
 int moe_device_status(void* workspace, void* stream, int32_t* status_out);

@@ -93,6 +93,8 @@ _SIGS = {
                                        ctypes.POINTER(moe_stats), _P, ctypes.c_size_t, _P,
                                        ctypes.POINTER(moe_timing)]),
     "moe_selftest_timeout": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_uint32, _P]),
+    "moe_selftest_barrier_timeout": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_uint32,
+                                                    ctypes.c_uint32, _P]),
     "moe_device_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "moe_kernel_launches": (ctypes.c_int64, []),
 }
@@ -259,6 +261,12 @@ def moe_selftest_timeout(workspace, limit_us, stream=None) -> int:
     return _check("moe_selftest_timeout", lib().moe_selftest_timeout(
         _ptr(workspace), workspace.numel() * workspace.element_size(), int(limit_us),
         _stream(stream)))
+
+
+def moe_selftest_barrier_timeout(workspace, limit_us, n_barriers, stream=None) -> int:
+    return _check("moe_selftest_barrier_timeout", lib().moe_selftest_barrier_timeout(
+        _ptr(workspace), workspace.numel() * workspace.element_size(), int(limit_us),
+        int(n_barriers), _stream(stream)))
 
 
 def moe_device_status(workspace, stream=None) -> int:

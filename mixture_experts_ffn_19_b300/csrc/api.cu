@@ -446,6 +446,19 @@ int moe_selftest_timeout(void* ws, size_t ws_bytes, uint32_t limit_us, void* str
              : MOE_ERR_CUDA;
 }
 
+int moe_selftest_barrier_timeout(void* ws, size_t ws_bytes, uint32_t limit_us,
+                                 uint32_t n_barriers, void* stream) {
+  if (!ws || !aligned16(ws) || ws_bytes < 16 + sizeof(GridBarrier)) return MOE_ERR_INVALID_ARG;
+  if (limit_us < 1 || limit_us > 1000000) return MOE_ERR_INVALID_ARG;
+  if (n_barriers < 1 || n_barriers > 4096) return MOE_ERR_INVALID_ARG;
+  // the status word is the workspace's first 4 bytes; the barrier state sits at byte 16
+  GridBarrier* bar = reinterpret_cast<GridBarrier*>(static_cast<char*>(ws) + 16);
+  return launch_barrier_selftest(static_cast<int*>(ws), bar, (uint64_t)limit_us * 1000ull,
+                                 (int)n_barriers, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
 int moe_device_status(void* ws, void* stream, int32_t* status_out) {
   if (!ws || !status_out) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

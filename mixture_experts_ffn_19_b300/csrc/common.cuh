@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "grid_barrier.h"
+
 namespace moe {
 
 // Device status codes (the workspace status word).  0 = ok.
@@ -139,6 +141,54 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       }
     }
   }
+}
+
+// ---------------------------------------------------------------- grid barrier
+
+// Grid-wide barrier for a cooperative launch (every CTA co-resident).  Bounded:
+// a CTA that waits longer than limit_ns records kDevTimeout, raises the abort
+// flag and returns false; a CTA that finds the flag raised, on entry or while
+// waiting, returns false at once, so a stalled grid costs one limit in all,
+// not one per barrier.  After false the caller must leave the kernel: the
+// counters no longer describe the grid.
+__device__ inline bool grid_barrier(GridBarrier* b, int* status, uint64_t limit_ns = kWaitLimitNs) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    volatile unsigned* gen = &b->gen;
+    volatile int* abort_flag = &b->abort;
+    if (*abort_flag) {
+      ok = 0;
+    } else {
+      const unsigned g = *gen;
+      __threadfence();
+      const unsigned arrived = atomicAdd(&b->count, 1u);
+      if (arrived == gridDim.x - 1) {
+        atomicExch(&b->count, 0u);
+        __threadfence();
+        atomicAdd(&b->gen, 1u);
+      } else {
+        const uint64_t t0 = globaltimer_ns();
+        while (*gen == g) {
+          if (*abort_flag) { ok = 0; break; }
+          __nanosleep(64);
+          if (globaltimer_ns() - t0 > limit_ns) {
+            set_status(status, kDevTimeout);
+            atomicExch(&b->abort, 1);
+            ok = 0;
+            break;
+          }
+        }
+      }
+    }
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  const bool ok = s_ok != 0;
+  __threadfence();
+  return ok;
 }
 
 // ---------------------------------------------------------------- TMA

@@ -161,36 +161,11 @@ __global__ void __launch_bounds__(kPlanThreads) dispatch_plan_kernel(DispatchPar
     int s = 0;
     for (int w = 0; w < kPlanThreads / 32; ++w) s += warp_tot[w];
     p.rr->primary_kept = s;
-    p.rr->bar_count = 0;
-    p.rr->bar_gen = 0;
+    p.rr->bar.count = 0;
+    p.rr->bar.gen = 0;
+    p.rr->bar.abort = 0;
   }
   for (int r = tid; r < kMaxRounds; r += kPlanThreads) p.rr->any_prop[r] = 0;
-}
-
-// Grid-wide barrier for a cooperative launch (all CTAs co-resident).  Bounded:
-// after kWaitLimitNs the waiting CTA records kDevTimeout and gives up.
-__device__ void grid_barrier(RerouteState* rr, int* status) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    volatile unsigned* gen = &rr->bar_gen;
-    const unsigned g = *gen;
-    __threadfence();
-    const unsigned arrived = atomicAdd(&rr->bar_count, 1u);
-    if (arrived == gridDim.x - 1) {
-      atomicExch(&rr->bar_count, 0u);
-      __threadfence();
-      atomicAdd(&rr->bar_gen, 1u);
-    } else {
-      const uint64_t t0 = globaltimer_ns();
-      while (*gen == g) {
-        __nanosleep(64);
-        if (globaltimer_ns() - t0 > kWaitLimitNs) { set_status(status, kDevTimeout); break; }
-      }
-    }
-    __threadfence();
-  }
-  __syncthreads();
-  __threadfence();
 }
 
 __global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchParams p) {
@@ -327,7 +302,8 @@ __global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchPa
       }
       if (__syncthreads_or(any) && tid == 0) atomicExch(&rr->any_prop[round], 1);
     }
-    grid_barrier(rr, p.status);
+    // a barrier that timed out (status recorded) ends the kernel for every CTA
+    if (!grid_barrier(&rr->bar, p.status)) return;
     if (!__ldcg(&rr->any_prop[round])) break;    // nothing proposed: every slot is placed or dropped
     // ---- phase B: per-expert exclusive scan over chunks (a warp per expert),
     //      next fill levels
@@ -339,7 +315,7 @@ __global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchPa
         if (lane == 0) rr->fill[cur ^ 1][e] = min(C, __ldcg(&rr->fill[cur][e]) + carry);
       }
     }
-    grid_barrier(rr, p.status);
+    if (!grid_barrier(&rr->bar, p.status)) return;
     // ---- phase C: acceptance in token order while the expert has room
     for (int e = tid; e < E; e += kRrThreads) fill_s[e] = __ldcg(&rr->fill[cur][e]);
     __syncthreads();

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "grid_barrier.h"
+
 namespace moe {
 
 constexpr int kAlign = 128;        // rows per expert segment granule (= GEMM tile M)
@@ -43,6 +45,8 @@ cudaError_t launch_quantize_fp8(const void* w, int n_mat, int64_t per_mat, uint8
                                 int num_sms, cudaStream_t s);
 
 cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t s);
+cudaError_t launch_barrier_selftest(int* status, GridBarrier* bar, uint64_t limit_ns,
+                                    int n_barriers, cudaStream_t s);
 
 cudaError_t launch_bias_update(const int* picks, float* bias, int N, int E, int k, float gamma,
                                cudaStream_t s);
@@ -66,7 +70,7 @@ struct RerouteState {
   int fill[2][kMaxExperts];      // per-expert fill levels, double-buffered by round
   int any_prop[kMaxRounds];      // round r made at least one proposal
   int primary_kept;
-  unsigned bar_count, bar_gen;   // grid barrier
+  GridBarrier bar;               // grid barrier of the cooperative kernel
 };
 size_t reroute_scratch_ints(int N, int k, int E);
 

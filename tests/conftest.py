@@ -29,3 +29,19 @@ def cuda():
     import mixture_experts_ffn_19_b300 as moe
     moe.lib()
     return torch.device("cuda:0")
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Print the parity figures the GPU tests measured (norm-wise and element-wise
+    error, near-ties and flips per case)."""
+    try:
+        from helpers import PARITY_REPORT
+    except ImportError:
+        return
+    if not PARITY_REPORT:
+        return
+    tr = terminalreporter
+    tr.section("parity report")
+    for name, f in PARITY_REPORT:
+        tr.write_line(name + ": " + ", ".join(
+            f"{k} {v:.3g}" if isinstance(v, float) else f"{k} {v}" for k, v in f.items()))

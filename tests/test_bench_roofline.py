@@ -49,3 +49,31 @@ def test_kernel_rule():
     assert names["decode_mixtral"] == names["decode_dsv2"] == "ffn_tc_swap_kernel<0>"
     assert names["decode_mixtral_fp8"] == names["decode_dsv2_fp8"] == "ffn_tc_swap_kernel<0,fp8>"
     assert names["tiny_fp32"] == "ffn_simt_kernel<1>"
+
+
+def test_tensor_peak_rule():
+    """The burst peak for a short timed region or one that ran uncapped; the
+    sustained peak only for a second or more under the power cap."""
+    pk = {"bf16_tflops": 1808.6, "bf16_tflops_sustained": 1390.4, "hbm_gbs": 6425.0,
+          "source": "measured"}
+    assert bench.tensor_peak(pk, 0.43, {"reasons": ["sw_power_cap"]})[0] == 1808.6
+    assert bench.tensor_peak(pk, 0.43, {"reasons": []})[0] == 1808.6
+    assert bench.tensor_peak(pk, 5.0, {"reasons": []})[0] == 1808.6
+    assert bench.tensor_peak(pk, 5.0, {"reasons": ["sw_power_cap"]})[0] == 1390.4
+    assert "burst" in bench.tensor_peak(pk, 0.43, {"reasons": None})[1]
+
+
+def test_gemm1_roofline_picks_binding_bound():
+    pk = {"bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "hbm_gbs": 6400.0,
+          "source": "measured"}
+    w = synth.WORKLOADS["mixtral_prefill"]
+    counts = np.full(8, 1024)
+    flop = 2 * 8192 * 4096 * 2 * 14336
+    r = bench.gemm1_roofline(w, counts, 8192, flop, 1.36, 0.43, {"sm_mhz": 2032,
+                                                                    "reasons": []}, pk)
+    assert r["bound"] == "tensor" and r["peak"] == 1800.0
+    assert abs(r["frac"] - flop / 1.36e-3 / 1e12 / 1800.0) < 1e-12
+    wd = synth.WORKLOADS["decode_mixtral"]
+    r2 = bench.gemm1_roofline(wd, np.full(8, 16), 128, 2 * 128 * 4096 * 2 * 14336, 0.33, 0.1,
+                              {"sm_mhz": 2032, "reasons": []}, pk)
+    assert r2["bound"] == "hbm" and r2["unit"] == "GB/s"

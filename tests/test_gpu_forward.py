@@ -6,7 +6,8 @@ import torch
 import mixture_experts_ffn_19_b300 as moe
 import oracle
 import synth
-from helpers import config_of, rel_err_inf, to_dev, to_f64
+from helpers import (NEAR_TIE, adopt_near_ties, config_of, elementwise_err, rel_err_inf,
+                     report, to_dev, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -46,30 +47,35 @@ def view_f32(ws, ptr, n):
 
 
 def check_forward(w, inp, g, tokens=None):
+    """Routing integers bit-exact and y within tolerance for every token.
+
+    A top-k that differs from the oracle's must belong to a counted near-tie
+    (oracle margin < 1e-6) and be one of that tie's valid selections; the
+    oracle is then re-run under the device's resolution of those ties, and
+    capacity, layout and every output row are compared under it."""
     o = oracle.moe_forward(w, inp, tokens=tokens)
     N, k = w.n_tokens, w.top_k
     ws, v = g["ws"], g["views"]
     idx = view_i32(ws, v.topk_idx, N * k).reshape(N, k)
     final = view_i32(ws, v.final_idx, N * k).reshape(N, k)
-    near = o["margin"] < 1e-6
-    routing_same = np.all(idx == o["idx"], axis=1) & np.all(final == o["final"], axis=1)
-    bad = np.nonzero(~routing_same)[0]
-    print(f"{w.name}: near-ties {near.sum()}, routing mismatches {len(bad)}")
-    if near.sum() == 0:
-        assert len(bad) == 0, f"routing differs on tokens {bad[:10]}"
+    adopted, flips = adopt_near_ties(o, idx)
+    near = int((o["margin"] < NEAR_TIE).sum())
+    if len(flips):
+        o = oracle.moe_forward(w, inp, tokens=tokens, idx_given=adopted)
+    print(f"{w.name}: near-ties {near}, flipped {len(flips)}")
+    np.testing.assert_array_equal(final, o["final"])
     toks = o["tokens"]
     y = to_f64(g["y"])[toks]
-    keep = routing_same[toks]
-    err = rel_err_inf(y[keep], o["y"][keep])
+    err = rel_err_inf(y, o["y"])
     tol = 1e-4 if w.dtype == synth.DT_F32 else 2e-2
-    print(f"{w.name}: y rel err {err:.3g} over {keep.sum()} tokens")
+    report(f"forward {w.name} N={N} E={w.n_experts} k={k}", tokens=len(toks), rel_err_inf=err,
+           elementwise_err=elementwise_err(y, o["y"]), near_ties=near, flipped=len(flips))
     assert err <= tol
     s = g["stats"]
     np.testing.assert_allclose(s["mean_prob"], o["mean_prob"], rtol=1e-5, atol=1e-9)
     np.testing.assert_allclose(s["l_bal"][0], o["l_bal"], rtol=1e-5)
-    if len(bad) == 0:
-        np.testing.assert_array_equal(s["counts"], o["counts"])
-        assert s["n_dropped"][0] == o["n_dropped"] and s["n_rerouted"][0] == o["n_rerouted"]
+    np.testing.assert_array_equal(s["counts"], o["counts"])
+    assert s["n_dropped"][0] == o["n_dropped"] and s["n_rerouted"][0] == o["n_rerouted"]
     return o
 
 

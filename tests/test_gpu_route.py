@@ -6,7 +6,7 @@ import torch
 import mixture_experts_ffn_19_b300 as moe
 import oracle
 import synth
-from helpers import config_of, to_dev
+from helpers import config_of, report, to_dev, valid_selection
 
 pytestmark = pytest.mark.gpu
 
@@ -43,8 +43,13 @@ def check_route(w, inp, g):
     mism = np.nonzero(~same)[0]
     print(f"{w.name}: near-tie tokens {near.sum()}, index mismatches {len(mism)}, "
           f"max |dp| {np.max(np.abs(g['p'] - r['key'])):.3g}")
-    # every mismatch must be a counted near-tie
+    # every mismatch must be a counted near-tie, resolved in one of its valid ways
     assert np.all(near[mism]), f"mismatch on non-near-tie tokens {mism[~near[mism]][:10]}"
+    for t in mism:
+        assert valid_selection(r["key"][t], g["idx"][t]), f"token {t}: invalid selection"
+    report(f"route {w.name} N={w.n_tokens} E={w.n_experts} k={w.top_k}",
+           near_ties=int(near.sum()), flipped=len(mism),
+           max_abs_dp=float(np.max(np.abs(g["p"] - r["key"]))))
     ok = same & ~near
     np.testing.assert_allclose(g["w"][ok], r["w"][ok], rtol=1e-5, atol=1e-7)
     # probs holds the selection scores: p, or p + b under selection-only bias
