@@ -297,9 +297,11 @@ int moe_forward_fp8(const moe_config* cfg, const void* x, const void* w_router,
  * arguments and results as moe_dispatch, with the scratch kept in a fixed
  * 8 MiB device array inside the library, which every GPU that loads the
  * library holds until exit; nothing is allocated.
- *   device_status  [1] int32 out, nullable: cleared by the call, then set to a
- *                  nonzero code by a device-side failure (1 = a wait timed
- *                  out, 2 = a bad expert index or internal check).
+ *   device_status  [1] int32 device pointer, required (MOE_ERR_INVALID_ARG if
+ *                  null): cleared by the call, then set to a nonzero code by
+ *                  a device-side failure (1 = a wait timed out, 2 = a bad
+ *                  expert index or internal check).  It is the only place
+ *                  such a failure is reported.
  * Returns MOE_ERR_WORKSPACE when the scratch for these sizes exceeds 8 MiB
  * (about 60k tokens at E=256, k=8).  The first call on a device looks up the
  * array's address (cudaGetSymbolAddress, once per device): make it before any

@@ -60,7 +60,7 @@ cudaError_t scratch_address(void** out) {
 size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
 struct ScratchLayout {
-  size_t status, chunk_cnt, local_rank, slot, rr_state, rr_scratch, total;
+  size_t chunk_cnt, local_rank, slot, rr_state, rr_scratch, total;
 };
 
 ScratchLayout scratch_layout(const moe_config* c) {
@@ -68,7 +68,6 @@ ScratchLayout scratch_layout(const moe_config* c) {
   const size_t N = (size_t)c->n_tokens, k = (size_t)c->top_k, E = (size_t)c->n_experts;
   size_t off = 0;
   auto take = [&](size_t bytes) { const size_t o = off; off = up256(off + bytes); return o; };
-  L.status = take(sizeof(int32_t));
   L.chunk_cnt = take((N + kRankTC - 1) / kRankTC * E * 4);
   L.local_rank = take(N * k * 4);
   L.slot = take(N * k * 4);
@@ -91,7 +90,9 @@ extern "C" int moe_dispatch_noalloc(const moe_config* cfg, const int32_t* topk_i
   using namespace moe;
   int st = moe_validate_config(cfg);
   if (st != MOE_OK) return st;
-  if (!topk_idx || !x || !final_idx || !pos || !offsets || !perm || !x_perm)
+  // device_status is required: the scratch array is not readable through any
+  // entry point, so a failure recorded there would go unreported
+  if (!topk_idx || !x || !final_idx || !pos || !offsets || !perm || !x_perm || !device_status)
     return MOE_ERR_INVALID_ARG;
   if (cfg->cap_mode == MOE_CAP_REROUTE && !probs) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_INVALID_ARG;
@@ -100,7 +101,7 @@ extern "C" int moe_dispatch_noalloc(const moe_config* cfg, const int32_t* topk_i
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* base = nullptr;
   if (scratch_address(reinterpret_cast<void**>(&base)) != cudaSuccess) return MOE_ERR_CUDA;
-  int* status = device_status ? device_status : reinterpret_cast<int*>(base + L.status);
+  int* status = device_status;
   if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cfg->n_tokens == 0) return MOE_OK;
 

@@ -88,6 +88,11 @@ def test_noalloc_dispatch_matches_workspace_dispatch(cuda, w):
 def test_noalloc_rejects_sizes_beyond_its_scratch(cuda):
     f = _noalloc()
     cfg = moe.make_config(1 << 20, 64, 256, 8, 64, cap_mode=moe.MOE_CAP_REROUTE, alpha=1.0)
-    st = f(ctypes.byref(cfg), 16, 16, 16, 16, 16, 16, 16, 16, None, None,
+    st = f(ctypes.byref(cfg), 16, 16, 16, 16, 16, 16, 16, 16, None, 16,
            torch.cuda.current_stream().cuda_stream)
     assert st == moe.MOE_ERR_WORKSPACE
+    # a null device_status is refused: device-side failures would go unreported
+    small = moe.make_config(64, 64, 8, 2, 64)
+    st = f(ctypes.byref(small), 16, 16, 16, 16, 16, 16, 16, 16, None, None,
+           torch.cuda.current_stream().cuda_stream)
+    assert st == moe.MOE_ERR_INVALID_ARG
