@@ -36,7 +36,7 @@ def _worker(rank, world, port, out):
 
 def test_two_rank_replicas_host_logic():
     world = 2
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
     assert out[0][0] == out[1][0] == 15.0                # max over ranks

@@ -167,7 +167,7 @@ EP_CASES = [
 @pytest.mark.parametrize("wname,overrides", EP_CASES, ids=[c[0] for c in EP_CASES])
 def test_two_rank_expert_parallel_layer_equals_one_device(wname, overrides):
     world = 2
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.spawn(_rank_main, args=(world, _free_port(), wname, overrides, out), nprocs=world,
              join=True)
