@@ -22,7 +22,7 @@ int64_t align_rows(int64_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Layout {
-  size_t status, acc_p, acc_pick, ticket, acc_zh, zero_end;  // [status .. zero_end) is cleared per call
+  size_t status, acc_p, acc_pick, ticket, acc_zh, tile_ctr, zero_end;  // [status .. zero_end) is cleared per call
   size_t topk_idx, topk_w, probs, final_idx, slot, pos, offsets, counts, perm;
   size_t part, chunk_cnt, local_rank, rr_state, rr_scratch;
   size_t x_perm, h, y_perm, total;
@@ -48,6 +48,7 @@ Layout layout_of(const moe_config* c) {
   L.acc_pick = take(E * 4);
   L.ticket = take(4);
   L.acc_zh = take(2 * 8);
+  L.tile_ctr = take(2 * 4);
   L.zero_end = off;
   L.topk_idx = take(N * k * 4);
   L.topk_w = take(N * k * 4);
@@ -157,6 +158,7 @@ int ffn_impl(const moe_config* c, const void* x, const void* x_perm, const int32
   fp.h = at<void>(ws, L.h); fp.y_perm = y_perm;
   fp.max_rows = max_rows_of(c); fp.max_total_rows = max_total_rows_of(c);
   fp.status = at<int>(ws, L.status);
+  fp.tile_ctr = at<int>(ws, L.tile_ctr);
   fp.num_sms = num_sms();
   fp.w_scales = w_scales;
   const cudaError_t err = c->dtype == MOE_BF16 ? launch_ffn_tc(fp, s, mid) : launch_ffn_simt(fp, s, mid);

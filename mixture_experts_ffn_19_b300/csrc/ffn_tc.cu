@@ -38,6 +38,13 @@ namespace {
 constexpr int BM = 128, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int NUM_THREADS = 192;
+// Below this many tiles per CTA the sum of a CTA's tile times varies too much
+// for a fixed deal to finish every CTA together, so CTAs claim tiles as they go.
+#ifndef MOE_DYNAMIC_TILES_PER_CTA
+#define MOE_DYNAMIC_TILES_PER_CTA 32
+#endif
+constexpr int kDynamicTilesPerCta = MOE_DYNAMIC_TILES_PER_CTA;
+constexpr int QSLOTS = 4;                // tile-index queue from the TMA warp
 
 // Tile width BN (the MMA's N: output columns of a GEMM-2 tile, gate + up
 // columns of a GEMM-1 tile) and the depth of the shared-memory ring.
@@ -60,10 +67,13 @@ struct TileCfg {
     uint64_t empty[STAGES];
     uint64_t tfull[2];
     uint64_t tempty[2];
+    uint64_t qfull[QSLOTS];     // tile index published (dynamic claiming)
+    uint64_t qempty[QSLOTS];    // read by the MMA lane and the four epilogue warps
+    int q_tile[QSLOTS];
     uint32_t tmem_base;
     int abort;
     int total_mtiles;
-    int pad;
+    int dyn;
     int mt_prefix[kMaxExperts + 16];
   };
   static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctrl);
@@ -77,7 +87,9 @@ struct TcParams {
   const int32_t* offsets;
   __nv_bfloat16* out;
   int* status;
+  int* ctr;                              // [2] tile-claim and done counters (zero between launches)
 };
+
 
 struct TileCoord {
   int seg, m, n;
@@ -117,6 +129,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(&ctrl->full[s], 1); mbar_init(&ctrl->empty[s], 1); }
     for (int b = 0; b < 2; ++b) { mbar_init(&ctrl->tfull[b], 1); mbar_init(&ctrl->tempty[b], 128); }
+    for (int q = 0; q < QSLOTS; ++q) { mbar_init(&ctrl->qfull[q], 1); mbar_init(&ctrl->qempty[q], 5); }
     ctrl->abort = 0;
     int run = 0;
     for (int s = 0; s < nseg; ++s) {
@@ -125,6 +138,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ 
     }
     ctrl->mt_prefix[nseg] = run;
     ctrl->total_mtiles = run;
+    ctrl->dyn = p.ctr != nullptr && run * p.n_tiles_n < kDynamicTilesPerCta * (int)gridDim.x;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -140,10 +154,23 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ 
   const int KB = (p.K + BK - 1) / BK;
   volatile int* abort = &ctrl->abort;
 
+  const bool dyn = ctrl->dyn != 0;
+
   if (warp == 0) {
     if (lane == 0) {
-      uint32_t kc = 0;
-      for (int T = blockIdx.x; T < total_tiles && !*abort; T += gridDim.x) {
+      uint32_t kc = 0, qi = 0;
+      // tiles in the static order T, T + grid, ...; or (dynamic) the first
+      // wave in that order, then whatever tile the shared counter hands out,
+      // each index published to the MMA and epilogue roles through the queue
+      for (int T = blockIdx.x;; ++qi) {
+        if (T >= total_tiles || *abort) T = -1;
+        if (dyn) {
+          const int slot = qi % QSLOTS;
+          if (!mbar_wait(&ctrl->qempty[slot], ((qi / QSLOTS) & 1) ^ 1, abort, p.status)) break;
+          ctrl->q_tile[slot] = T;
+          mbar_arrive(&ctrl->qfull[slot]);
+        }
+        if (T < 0) break;
         const TileCoord tc = tile_coord(ctrl, nseg, p.n_tiles_n, T);
         const CUtensorMap* amap = &tmA0;
         int a_row = p.offsets[tc.seg] + tc.m * BM;
@@ -164,12 +191,21 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ 
             tma_load_2d(b_s, &tmB0, &ctrl->full[st], kb * BK, b_row);
           }
         }
+        T = dyn ? (int)gridDim.x + atomicAdd(&p.ctr[0], 1) : T + (int)gridDim.x;
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      uint32_t kc = 0, it = 0;
-      for (int T = blockIdx.x; T < total_tiles && !*abort; T += gridDim.x, ++it) {
+      uint32_t kc = 0;
+      for (uint32_t it = 0;; ++it) {
+        int T = blockIdx.x + (int)(it * gridDim.x);
+        if (dyn) {
+          const int slot = it % QSLOTS;
+          if (!mbar_wait(&ctrl->qfull[slot], (it / QSLOTS) & 1, abort, p.status)) break;
+          T = ctrl->q_tile[slot];
+          mbar_arrive(&ctrl->qempty[slot]);
+        }
+        if (T < 0 || T >= total_tiles || *abort) break;
         const uint32_t buf = it & 1, use = it >> 1;
         if (!mbar_wait(&ctrl->tempty[buf], (use & 1) ^ 1, abort, p.status)) break;
         tc_fence_after();
@@ -195,9 +231,18 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ 
   } else {
     // epilogue warps 2..5: TMEM lane quarter = warp % 4
     const int q = warp & 3;
-    uint32_t it = 0;
-    for (int T = blockIdx.x; T < total_tiles; T += gridDim.x, ++it) {
+    for (uint32_t it = 0;; ++it) {
       if (__any_sync(0xffffffffu, *abort != 0)) break;
+      int T = blockIdx.x + (int)(it * gridDim.x);
+      if (dyn) {
+        const int slot = it % QSLOTS;
+        const bool got = mbar_wait(&ctrl->qfull[slot], (it / QSLOTS) & 1, abort, p.status);
+        if (!__all_sync(0xffffffffu, got)) break;
+        T = ctrl->q_tile[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctrl->qempty[slot]);
+      }
+      if (T < 0 || T >= total_tiles) break;
       const TileCoord tc = tile_coord(ctrl, nseg, p.n_tiles_n, T);
       const uint32_t buf = it & 1, use = it >> 1;
       const bool ok = mbar_wait(&ctrl->tfull[buf], use & 1, abort, p.status);
@@ -256,6 +301,14 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ 
   if (warp == 1) {
     __syncwarp();
     tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+  // the last CTA to finish leaves the counters at zero for the next launch
+  if (dyn && threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&p.ctr[1], 1) == (int)gridDim.x - 1) {
+      atomicExch(&p.ctr[0], 0);
+      atomicExch(&p.ctr[1], 0);
+    }
   }
 }
 
@@ -767,7 +820,7 @@ cudaError_t launch_prefill(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) 
       !make_map(&b1, p.w_up, (uint64_t)ET * p.F, p.d, BN / 2))
     return cudaErrorInvalidValue;
   TcParams t1{p.E, p.S, p.d, p.F, (p.F + BN / 2 - 1) / (BN / 2), BN / 2, p.offsets,
-              static_cast<__nv_bfloat16*>(p.h), p.status};
+              static_cast<__nv_bfloat16*>(p.h), p.status, p.tile_ctr};
   ffn_tc_kernel<0, C><<<p.num_sms, NUM_THREADS, C::SMEM_BYTES, s>>>(a0, a1, b0, b1, t1);
   count_launch();
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
@@ -776,8 +829,10 @@ cudaError_t launch_prefill(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) 
   if (!make_map(&a0, p.h, (uint64_t)p.max_total_rows, p.F, BM) ||
       !make_map(&b0, p.w_down, (uint64_t)ET * p.d, p.F, BN))
     return cudaErrorInvalidValue;
+  // GEMM-2's tiles cost the same whatever the segment (no SwiGLU, weights
+  // shared by every row tile of a segment): the static deal measured faster
   TcParams t2{p.E, p.S, p.F, p.d, (p.d + BN - 1) / BN, BN, p.offsets,
-              static_cast<__nv_bfloat16*>(p.y_perm), p.status};
+              static_cast<__nv_bfloat16*>(p.y_perm), p.status, nullptr};
   ffn_tc_kernel<1, C><<<p.num_sms, NUM_THREADS, C::SMEM_BYTES, s>>>(a0, a0, b0, b0, t2);
   count_launch();
   return cudaGetLastError();

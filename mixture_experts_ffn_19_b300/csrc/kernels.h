@@ -113,6 +113,7 @@ struct FfnParams {
   void* y_perm;              // [max_total_rows, d]
   int64_t max_rows, max_total_rows;
   int* status;
+  int* tile_ctr;             // [2] zeroed ints: GEMM-1's tile-claim and done counters
   int num_sms;
   // E4M3 weights: w_gate / w_up / w_down hold codes and w_scales [3][E+S] the
   // gate, up and down scale of each expert; null for bf16 weights
