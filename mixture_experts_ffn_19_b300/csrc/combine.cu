@@ -46,19 +46,32 @@ struct Vec<float> {
 
 template <typename T>
 __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
+  griddep_begin();
   constexpr int VN = Vec<T>::n;
   const int t = blockIdx.x;
   __shared__ int rows[kMaxTopk + 8];
   __shared__ float gates[kMaxTopk + 8];
   __shared__ int nrows;
-  if (threadIdx.x == 0) {
-    int n = 0;
-    for (int s = 0; s < p.S; ++s) { rows[n] = p.offsets[p.E + s] + t; gates[n] = 1.f; ++n; }
-    for (int j = 0; j < p.k; ++j) {
-      const size_t a = (size_t)t * p.k + j;
-      if (p.final_idx[a] >= 0) { rows[n] = p.pos[a]; gates[n] = p.topk_w[a]; ++n; }
+  if (threadIdx.x < 32) {
+    // lane i < S + k fetches contribution i (shared experts, then slots in
+    // order) in parallel; the kept ones are packed in that order
+    const int lane = threadIdx.x, nr = p.S + p.k;
+    int row = -1;
+    float g = 0.f;
+    if (lane < p.S) {
+      row = p.offsets[p.E + lane] + t;
+      g = 1.f;
+    } else if (lane < nr) {
+      const size_t a = (size_t)t * p.k + (lane - p.S);
+      if (p.final_idx[a] >= 0) { row = p.pos[a]; g = p.topk_w[a]; }
     }
-    nrows = n;
+    const unsigned kept = __ballot_sync(0xffffffffu, row >= 0);
+    if (row >= 0) {
+      const int at = __popc(kept & lanemask_lt());
+      rows[at] = row;
+      gates[at] = g;
+    }
+    if (lane == 0) nrows = __popc(kept);
   }
   __syncthreads();
   const int nvec = p.d / VN;
@@ -96,9 +109,11 @@ cudaError_t launch_combine(const CombineParams& p, bool bf16, cudaStream_t s) {
   const int vn = bf16 ? 8 : 4;
   const int nvec = p.d / vn;
   int threads = nvec < 256 ? ((nvec + 31) / 32) * 32 : 256;
-  if (bf16) { combine_kernel<__nv_bfloat16><<<p.N, threads, 0, s>>>(p); count_launch(); }
-  else { combine_kernel<float><<<p.N, threads, 0, s>>>(p); count_launch(); }
-  return cudaGetLastError();
+  const cudaError_t err = bf16 ? launch_chained(combine_kernel<__nv_bfloat16>, p.N, threads, 0, s, p)
+                               : launch_chained(combine_kernel<float>, p.N, threads, 0, s, p);
+  if (err != cudaSuccess) return err;
+  count_launch();
+  return cudaSuccess;
 }
 
 }  // namespace moe

@@ -32,6 +32,25 @@ __device__ __forceinline__ void set_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// ---------------------------------------------------------------- launch chaining
+
+// Kernels of the layer are launched with programmatic stream serialisation:
+// a kernel may start while its predecessor in the stream is still finishing.
+// Each calls griddep_wait() before it touches memory the predecessor may
+// write or read (it returns once the predecessor grid has completed and its
+// writes are visible; without the launch attribute it returns at once), then
+// griddep_launch_dependents() so that its own successor can be launched early.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_begin() {
+  griddep_wait();
+  griddep_launch_dependents();
+}
+
 // ---------------------------------------------------------------- numerics
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }

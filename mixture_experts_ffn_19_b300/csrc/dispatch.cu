@@ -29,6 +29,12 @@
 #include "common.cuh"
 #include "kernels.h"
 
+// When the row-copying dispatch kernels let their successor (the expert
+// GEMMs, one large CTA per SM) launch: at their start (1) or at their end (0).
+#ifndef MOE_DISPATCH_EARLY_TRIGGER
+#define MOE_DISPATCH_EARLY_TRIGGER 0
+#endif
+
 namespace moe {
 
 namespace {
@@ -61,6 +67,7 @@ __device__ int warp_exclusive_scan_column(int32_t* m, int n, int E, int e, int l
 }
 
 __global__ void __launch_bounds__(kRankTC) dispatch_rank_kernel(DispatchParams p) {
+  griddep_begin();
   extern __shared__ uint32_t bits[];             // [E][kRankTC/32]
   constexpr int W = kRankTC / 32;
   const int E = p.E, k = p.k;
@@ -126,6 +133,7 @@ __device__ void write_layout(const DispatchParams& p, const int* fill, int n_dro
 }
 
 __global__ void __launch_bounds__(kPlanThreads) dispatch_plan_kernel(DispatchParams p) {
+  griddep_begin();
   const int E = p.E, C = p.C;
   __shared__ int fill[kMaxExperts], total[kMaxExperts];
   __shared__ int warp_tot[kPlanThreads / 32];
@@ -350,6 +358,8 @@ __global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchPa
 
 template <typename T>
 __global__ void __launch_bounds__(128) dispatch_scatter_kernel(DispatchParams p) {
+  griddep_wait();
+  if (MOE_DISPATCH_EARLY_TRIGGER) griddep_launch_dependents();
   const int t = blockIdx.x;
   const int k = p.k, E = p.E;
   __shared__ int rows[kMaxTopk];
@@ -387,6 +397,98 @@ __global__ void __launch_bounds__(128) dispatch_scatter_kernel(DispatchParams p)
       if (row >= 0) dst[(size_t)row * nvec + v] = val;
     }
   }
+  if (!MOE_DISPATCH_EARLY_TRIGGER) griddep_launch_dependents();
+}
+
+// Small batches without reroute (N k <= kSmallAssign): the whole dispatch in
+// one launch, a CTA per token.  Every CTA reads all N k expert indices (a few
+// KB), so it knows the per-expert totals, and counts the earlier tokens that
+// hold each of its own experts: that count is the assignment's rank in token
+// order, the same rank the chunked rank/plan kernels produce.  CTA 0 writes
+// the segment layout; each CTA writes its own slots and copies its row.
+constexpr int kSmallThreads = 128;
+constexpr int kSmallAssign = 4096;
+
+template <typename T>
+__global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(DispatchParams p) {
+  griddep_wait();
+  if (MOE_DISPATCH_EARLY_TRIGGER) griddep_launch_dependents();
+  __shared__ int idx_s[kSmallAssign];
+  __shared__ int hist[kMaxExperts], fill[kMaxExperts], offs[kMaxExperts];
+  __shared__ int my_e[kMaxTopk], my_rank[kMaxTopk], rows[kMaxTopk];
+  __shared__ int s_dropped;
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+  const int E = p.E, k = p.k, nk = p.N * p.k;
+  for (int e = tid; e < E; e += kSmallThreads) hist[e] = 0;
+  if (tid < kMaxTopk) my_rank[tid] = 0;
+  if (tid == 0) s_dropped = 0;
+  __syncthreads();
+  for (int i = tid; i < nk; i += kSmallThreads) {
+    int e = p.topk_idx[i];
+    if (!valid_expert(e, E)) {          // not an expert index: record it, never index with it
+      if (i / k == t) set_status(p.status, kDevBadState);
+      e = -1;
+    }
+    idx_s[i] = e;
+    if (e >= 0) atomicAdd(&hist[e], 1);
+  }
+  __syncthreads();
+  if (tid < k) my_e[tid] = idx_s[t * k + tid];
+  for (int e = tid; e < E; e += kSmallThreads) {
+    fill[e] = min(hist[e], p.C);
+    if (hist[e] > fill[e]) atomicAdd(&s_dropped, hist[e] - fill[e]);
+  }
+  __syncthreads();
+  // rank of each own slot: earlier tokens holding the same expert (a token
+  // holds an expert at most once); integer sums, so the order does not matter
+  for (int j = 0; j < k; ++j) {
+    const int e = my_e[j];
+    if (e < 0) continue;
+    int c = 0;
+    for (int i = tid; i < t * k; i += kSmallThreads) c += idx_s[i] == e;
+    c = __reduce_add_sync(0xffffffffu, c);
+    if (lane == 0 && c) atomicAdd(&my_rank[j], c);
+  }
+  // segment starts: exclusive scan of the 128-row-padded fills (one warp)
+  if (tid < 32) {
+    int carry = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int v = e < E ? (fill[e] + kAlign - 1) / kAlign * kAlign : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (e < E) offs[e] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  __syncthreads();
+  if (tid < k) {
+    const int e = my_e[tid], r = my_rank[tid];
+    const size_t a = (size_t)t * k + tid;
+    int f = -1, row = -1;
+    if (e >= 0 && r < p.C) { f = e; row = offs[e] + r; }
+    p.final_idx[a] = f;
+    p.pos[a] = row;
+    if (row >= 0) p.perm[row] = t;
+    rows[tid] = row;
+  }
+  if (blockIdx.x == 0) write_layout(p, fill, s_dropped, 0);   // whole CTA
+  __syncthreads();
+  const int nvec = p.d * (int)sizeof(T) / 16;
+  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.x) + (size_t)t * p.d);
+  uint4* dst = reinterpret_cast<uint4*>(p.x_perm);
+  for (int v = tid; v < nvec; v += kSmallThreads) {
+    const uint4 val = src[v];
+    for (int j = 0; j < k; ++j) {
+      const int row = rows[j];
+      if (row >= 0) dst[(size_t)row * nvec + v] = val;
+    }
+  }
+  if (!MOE_DISPATCH_EARLY_TRIGGER) griddep_launch_dependents();
 }
 
 }  // namespace
@@ -397,15 +499,21 @@ size_t reroute_scratch_ints(int N, int k, int E) {
 }
 
 cudaError_t launch_dispatch(const DispatchParams& p, bool bf16, cudaStream_t s) {
+  cudaError_t err;
+  if (p.cap_mode != 2 && (int64_t)p.N * p.k <= kSmallAssign) {
+    err = bf16 ? launch_chained(dispatch_small_kernel<__nv_bfloat16>, p.N, kSmallThreads, 0, s, p)
+               : launch_chained(dispatch_small_kernel<float>, p.N, kSmallThreads, 0, s, p);
+    if (err != cudaSuccess) return err;
+    count_launch();
+    return cudaSuccess;
+  }
   const int W = kRankTC / 32;
-  dispatch_rank_kernel<<<p.n_chunks, kRankTC, sizeof(uint32_t) * p.E * W, s>>>(p);
-  count_launch();
-  cudaError_t err = cudaGetLastError();
+  err = launch_chained(dispatch_rank_kernel, p.n_chunks, kRankTC, sizeof(uint32_t) * p.E * W, s, p);
   if (err != cudaSuccess) return err;
-  dispatch_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
   count_launch();
-  err = cudaGetLastError();
+  err = launch_chained(dispatch_plan_kernel, 1, kPlanThreads, 0, s, p);
   if (err != cudaSuccess) return err;
+  count_launch();
   if (p.cap_mode == 2) {
     int dev = 0, sms = 0, per_sm = 0;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
@@ -425,9 +533,11 @@ cudaError_t launch_dispatch(const DispatchParams& p, bool bf16, cudaStream_t s) 
     if (err != cudaSuccess) return err;
     count_launch();
   }
-  if (bf16) { dispatch_scatter_kernel<__nv_bfloat16><<<p.N, 128, 0, s>>>(p); count_launch(); }
-  else { dispatch_scatter_kernel<float><<<p.N, 128, 0, s>>>(p); count_launch(); }
-  return cudaGetLastError();
+  err = bf16 ? launch_chained(dispatch_scatter_kernel<__nv_bfloat16>, p.N, 128, 0, s, p)
+             : launch_chained(dispatch_scatter_kernel<float>, p.N, 128, 0, s, p);
+  if (err != cudaSuccess) return err;
+  count_launch();
+  return cudaSuccess;
 }
 
 }  // namespace moe

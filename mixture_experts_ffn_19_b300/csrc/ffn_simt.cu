@@ -37,6 +37,7 @@ __device__ int find_segment(const int32_t* offsets, int nseg, int r) {
 // STAGE 2: Y = H W2^T + b2
 template <int STAGE, bool SWIGLU>
 __global__ void __launch_bounds__(256) ffn_simt_kernel(FfnParams p) {
+  griddep_begin();
   __shared__ __align__(16) float As[kBK][kBM + kPad];
   __shared__ __align__(16) float Bs[kBK][kBN + kPad];
   __shared__ __align__(16) float Us[SWIGLU && STAGE == 1 ? kBK : 1][kBN + kPad];
@@ -129,14 +130,14 @@ __global__ void __launch_bounds__(256) ffn_simt_kernel(FfnParams p) {
 cudaError_t launch_ffn_simt(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) {
   const int mt = (int)((p.max_total_rows + kBM - 1) / kBM);
   dim3 g1(mt, (p.F + kBN - 1) / kBN), g2(mt, (p.d + kBN - 1) / kBN);
-  if (p.act == 1) { ffn_simt_kernel<1, true><<<g1, 256, 0, s>>>(p); count_launch(); }
-  else { ffn_simt_kernel<1, false><<<g1, 256, 0, s>>>(p); count_launch(); }
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = p.act == 1 ? launch_chained(ffn_simt_kernel<1, true>, g1, 256, 0, s, p)
+                                : launch_chained(ffn_simt_kernel<1, false>, g1, 256, 0, s, p);
   if (err != cudaSuccess) return err;
-  if (mid) cudaEventRecord(mid, s);
-  ffn_simt_kernel<2, false><<<g2, 256, 0, s>>>(p);
   count_launch();
-  return cudaGetLastError();
+  if (mid) cudaEventRecord(mid, s);
+  if ((err = launch_chained(ffn_simt_kernel<2, false>, g2, 256, 0, s, p)) != cudaSuccess) return err;
+  count_launch();
+  return cudaSuccess;
 }
 
 }  // namespace moe

@@ -31,6 +31,13 @@
 #include "common.cuh"
 #include "kernels.h"
 
+// When the GEMMs let their successor launch: at their start (1), or once a CTA
+// has finished its tiles (0), so that the successor's waiting CTAs do not sit
+// beside a GEMM that still runs.
+#ifndef MOE_GEMM_EARLY_TRIGGER
+#define MOE_GEMM_EARLY_TRIGGER 0
+#endif
+
 namespace moe {
 
 namespace {
@@ -115,6 +122,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
               const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
               TcParams p) {
+  griddep_wait();
+  if (MOE_GEMM_EARLY_TRIGGER) griddep_launch_dependents();
   constexpr int BN = C::BN, STAGES = C::STAGES, B_BYTES = C::B_BYTES;
   constexpr int STAGE_BYTES = C::STAGE_BYTES, TMEM_COLS = C::TMEM_COLS;
   constexpr uint32_t IDESC = C::IDESC;
@@ -297,6 +306,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ 
   }
   tc_fence_before();
   __syncthreads();
+  if (!MOE_GEMM_EARLY_TRIGGER) griddep_launch_dependents();
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
@@ -423,6 +433,8 @@ __global__ void __launch_bounds__(Shape<W8>::THREADS, 1)
 ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                    const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    Params p) {
+  griddep_wait();
+  if (MOE_GEMM_EARLY_TRIGGER) griddep_launch_dependents();
   // tmB0/tmB1: token rows (x_perm / x for GEMM-1, H for GEMM-2);
   // tmA0/tmA1: weights (gate / up for GEMM-1, down for GEMM-2), bf16 or E4M3
   constexpr int STAGES = Shape<W8>::STAGES, STAGE_BYTES = Shape<W8>::STAGE_BYTES;
@@ -694,6 +706,7 @@ ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_consta
   }
   tc_fence_before();
   __syncthreads();
+  if (!MOE_GEMM_EARLY_TRIGGER) griddep_launch_dependents();
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
@@ -783,9 +796,10 @@ cudaError_t launch_swap(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) {
   swp::Params t1{p.E, p.S, p.N, p.d, p.F, (p.F + 63) / 64, p.offsets, p.counts,
                  static_cast<__nv_bfloat16*>(p.h), p.status,
                  W8 ? p.w_scales : nullptr, W8 ? p.w_scales + ET : nullptr};
-  swp::ffn_tc_swap_kernel<0, W8><<<p.num_sms, THREADS, SMEM, s>>>(b0, b1, a0, a1, t1);
+  if ((err = launch_chained(swp::ffn_tc_swap_kernel<0, W8>, p.num_sms, THREADS, SMEM, s, b0, b1,
+                            a0, a1, t1)) != cudaSuccess)
+    return err;
   count_launch();
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
   if (mid) cudaEventRecord(mid, s);
   if (!make_map(&b0, p.h, (uint64_t)p.max_total_rows, p.F, swp::TOKB) ||
       !wmap(&a0, p.w_down, (uint64_t)ET * p.d, p.F, swp::BM))
@@ -793,9 +807,11 @@ cudaError_t launch_swap(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) {
   swp::Params t2{p.E, p.S, p.N, p.F, p.d, (p.d + swp::BM - 1) / swp::BM, p.offsets, p.counts,
                  static_cast<__nv_bfloat16*>(p.y_perm), p.status,
                  W8 ? p.w_scales + 2 * ET : nullptr, nullptr};
-  swp::ffn_tc_swap_kernel<1, W8><<<p.num_sms, THREADS, SMEM, s>>>(b0, b0, a0, a0, t2);
+  if ((err = launch_chained(swp::ffn_tc_swap_kernel<1, W8>, p.num_sms, THREADS, SMEM, s, b0, b0,
+                            a0, a0, t2)) != cudaSuccess)
+    return err;
   count_launch();
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -821,9 +837,10 @@ cudaError_t launch_prefill(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) 
     return cudaErrorInvalidValue;
   TcParams t1{p.E, p.S, p.d, p.F, (p.F + BN / 2 - 1) / (BN / 2), BN / 2, p.offsets,
               static_cast<__nv_bfloat16*>(p.h), p.status, p.tile_ctr};
-  ffn_tc_kernel<0, C><<<p.num_sms, NUM_THREADS, C::SMEM_BYTES, s>>>(a0, a1, b0, b1, t1);
+  if ((err = launch_chained(ffn_tc_kernel<0, C>, p.num_sms, NUM_THREADS, C::SMEM_BYTES, s, a0, a1,
+                            b0, b1, t1)) != cudaSuccess)
+    return err;
   count_launch();
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
   if (mid) cudaEventRecord(mid, s);
   // GEMM-2: A = H, B = down weights
   if (!make_map(&a0, p.h, (uint64_t)p.max_total_rows, p.F, BM) ||
@@ -833,9 +850,11 @@ cudaError_t launch_prefill(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) 
   // shared by every row tile of a segment): the static deal measured faster
   TcParams t2{p.E, p.S, p.F, p.d, (p.d + BN - 1) / BN, BN, p.offsets,
               static_cast<__nv_bfloat16*>(p.y_perm), p.status, nullptr};
-  ffn_tc_kernel<1, C><<<p.num_sms, NUM_THREADS, C::SMEM_BYTES, s>>>(a0, a0, b0, b0, t2);
+  if ((err = launch_chained(ffn_tc_kernel<1, C>, p.num_sms, NUM_THREADS, C::SMEM_BYTES, s, a0, a0,
+                            b0, b0, t2)) != cudaSuccess)
+    return err;
   count_launch();
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace

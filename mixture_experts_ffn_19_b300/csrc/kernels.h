@@ -9,6 +9,25 @@
 
 namespace moe {
 
+// Launch `kernel` on `s` with programmatic stream serialisation (the kernel
+// calls griddep_wait() before touching its predecessor's data), so its launch
+// and set-up overlap the predecessor's tail.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                           cudaStream_t s, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 constexpr int kAlign = 128;        // rows per expert segment granule (= GEMM tile M)
 constexpr int kRouteTM = 32;       // tokens per router CTA
 constexpr int kRankTC = 256;       // tokens per dispatch-rank CTA

@@ -35,6 +35,7 @@ __device__ __forceinline__ void load8f(const float* src, float (&v)[8]) {
 // folded into the running sum with Kahan compensation.
 template <int EJ>
 __global__ void __launch_bounds__(kThreads) route_logits_simt(RouteParams p, RouteSplit sp) {
+  griddep_begin();
   extern __shared__ __align__(16) float sm[];
   const int E = p.E, d = p.d, N = p.N;
   const int EP = EJ * 32;
@@ -122,6 +123,7 @@ __global__ void __launch_bounds__(kThreads) route_logits_simt(RouteParams p, Rou
 // Warp per token: logits from the partials, bias, softmax, top-k, gates.
 template <int EJ>
 __global__ void __launch_bounds__(kThreads) route_finish_kernel(RouteParams p, RouteSplit sp) {
+  griddep_begin();
   constexpr int EP = EJ * 32;
   __shared__ unsigned long long psum_w[kWarps][EP];
   __shared__ unsigned long long zh_w[kWarps][2];
@@ -298,16 +300,20 @@ cudaError_t launch_simt_t(const RouteParams& p, const RouteSplit& sp, cudaStream
   auto kern = route_logits_simt<EJ>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  kern<<<dim3((p.N + kTM - 1) / kTM, sp.ks), kThreads, smem, s>>>(p, sp);
+  if ((err = launch_chained(kern, dim3((p.N + kTM - 1) / kTM, sp.ks), kThreads, smem, s, p, sp)) !=
+      cudaSuccess)
+    return err;
   count_launch();
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 template <int EJ>
 cudaError_t launch_finish_t(const RouteParams& p, const RouteSplit& sp, cudaStream_t s) {
-  route_finish_kernel<EJ><<<route_finish_blocks(p.N), kThreads, 0, s>>>(p, sp);
+  const cudaError_t err =
+      launch_chained(route_finish_kernel<EJ>, route_finish_blocks(p.N), kThreads, 0, s, p, sp);
+  if (err != cudaSuccess) return err;
   count_launch();
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 #define MOE_EJ_SWITCH(E, F, ...)                  \

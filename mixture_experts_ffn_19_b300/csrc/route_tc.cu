@@ -46,6 +46,7 @@ struct Params {
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 route_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                 Params p) {
+  griddep_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -183,9 +184,11 @@ cudaError_t launch_route_logits_tc(const RouteSplit& s, const void* x, const voi
                                          (int)smem);
   if (err != cudaSuccess) return err;
   dim3 grid((N + BM - 1) / BM, s.ks);
-  route_logits_tc<<<grid, NUM_THREADS, smem, stream>>>(mx, mw, p);
+  if ((err = launch_chained(route_logits_tc, grid, NUM_THREADS, smem, stream, mx, mw, p)) !=
+      cudaSuccess)
+    return err;
   count_launch();
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace moe
