@@ -91,6 +91,9 @@ CASES = [
     synth.small_workload("e64_reroute", n_tokens=300, d_model=64, n_experts=8, top_k=2, alpha=0.3),
     synth.small_workload("dsv2", n_tokens=333, d_model=64, n_experts=160, top_k=6, n_shared=2),
     synth.small_workload("dsv2", n_tokens=1, d_model=64),
+    # either side of the one-kernel dispatch's limit (N k <= 4096, no reroute), with drops
+    synth.small_workload("mixtral_prefill", n_tokens=2048, d_model=64, alpha=0.7),
+    synth.small_workload("mixtral_prefill", n_tokens=2049, d_model=64, alpha=0.7),
     synth.small_workload("e64_reroute", n_tokens=2500, d_model=64, n_experts=256, top_k=8, alpha=1.0),
     # reroute ranked by p + b (selection-only bias)
     synth.small_workload("e64_reroute", n_tokens=1500, d_model=64, alpha=0.7,
