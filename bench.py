@@ -275,12 +275,25 @@ def oracle_experts(w, inp):
     if not w.fp8_weights:
         return None
     import oracle
+    cache = {}
 
     def get(e):
-        out = {"b1": None, "b2": None}
-        for key in ("w_gate", "w_up", "w_down"):
-            out[key] = oracle.quantize_fp8(inp[key][e])
-        return out
+        # quantised once per expert, as the library's weights are before timing
+        if e not in cache:
+            out = {"b1": None, "b2": None}
+            for key in ("w_gate", "w_up", "w_down"):
+                out[key] = oracle.quantize_fp8(inp[key][e])
+            cache[e] = out
+        return cache[e]
+    return get
+
+
+def prepared_experts(w, inp):
+    """oracle_experts with every expert prepared up front (outside any timing)."""
+    get = oracle_experts(w, inp)
+    if get is not None:
+        for e in range(w.n_experts + w.n_shared):
+            get(e)
     return get
 
 
@@ -293,7 +306,7 @@ def run_cpu_oracle(w, inp, budget_s=20.0, max_tokens=None):
     """Time the oracle (as it stands, on every host thread OpenMP gives it) on a
     bounded token sample; returns the cpu_baseline record (tokens/s)."""
     import oracle
-    get = oracle_experts(w, inp)
+    get = prepared_experts(w, inp)
     oracle.set_threads(oracle.hardware_concurrency())
     # grow the token sample until one timed run takes about a third of the budget
     n, dt = 1, 0.0
@@ -317,11 +330,12 @@ def run_cpu_oracle(w, inp, budget_s=20.0, max_tokens=None):
 def oracle_single_thread(w, inp):
     """The oracle on one thread over the workload's whole batch (seconds, tokens/s)."""
     import oracle
+    get = prepared_experts(w, inp)
     before = oracle.threads()
     oracle.set_threads(1)
     try:
         t0 = time.perf_counter()
-        oracle.moe_forward(w, inp, get_expert=oracle_experts(w, inp))
+        oracle.moe_forward(w, inp, get_expert=get)
         dt = time.perf_counter() - t0
     finally:
         oracle.set_threads(before)
@@ -339,7 +353,7 @@ def bench_reference(args, w):
     info = run_cpu_oracle(w, inp, budget_s=3 * budget, max_tokens=args.ref_tokens)
     n = int(info["sample"].split("first ")[1].split(" ")[0])
     per_step = []
-    get = oracle_experts(w, inp)
+    get = prepared_experts(w, inp)
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
         oracle.moe_forward(w, inp, tokens=np.arange(n), get_expert=get)
