@@ -98,7 +98,11 @@ typedef struct moe_config {
   int32_t act;             /* moe_act                                      */
   int32_t dtype;           /* moe_dtype                                    */
   int32_t cap_mode;        /* moe_cap_mode                                 */
-  float alpha;             /* capacity factor (> 0 unless MOE_CAP_NONE)    */
+  double alpha;            /* capacity factor (> 0 unless MOE_CAP_NONE), in
+                            * double: floor(floor(kN/E) * alpha) must see
+                            * the factor as written (0.7 as a float is
+                            * 0.69999999, which turns 1250 * 0.7 = 875
+                            * into 874)                                   */
   int32_t has_ffn_bias;    /* GELU experts: b1 [E+S, F], b2 [E+S, d]       */
   int32_t has_router_bias; /* router_bias [E] fp32 is given                */
   int32_t bias_mode;       /* moe_bias_mode (with has_router_bias)         */

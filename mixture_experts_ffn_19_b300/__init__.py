@@ -41,7 +41,7 @@ class moe_config(ctypes.Structure):
                 ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
                 ("d_ff", ctypes.c_int32), ("n_shared", ctypes.c_int32),
                 ("act", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("cap_mode", ctypes.c_int32), ("alpha", ctypes.c_float),
+                ("cap_mode", ctypes.c_int32), ("alpha", ctypes.c_double),
                 ("has_ffn_bias", ctypes.c_int32), ("has_router_bias", ctypes.c_int32),
                 ("bias_mode", ctypes.c_int32)]
 

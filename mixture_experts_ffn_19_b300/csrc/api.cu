@@ -77,7 +77,7 @@ T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws)
 int capacity_of(const moe_config* c) {
   if (c->cap_mode == MOE_CAP_NONE) return INT32_MAX;
   const double base = (double)(((int64_t)c->top_k * c->n_tokens) / c->n_experts);
-  const double cap = floor(base * (double)c->alpha);
+  const double cap = floor(base * c->alpha);
   return cap >= (double)INT32_MAX ? INT32_MAX : (int)cap;
 }
 
@@ -270,7 +270,7 @@ int moe_validate_config(const moe_config* c) {
   if (c->act != MOE_ACT_GELU && c->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (c->cap_mode < MOE_CAP_NONE || c->cap_mode > MOE_CAP_REROUTE) return MOE_ERR_INVALID_ARG;
-  if (c->cap_mode != MOE_CAP_NONE && !(c->alpha > 0.f && isfinite(c->alpha)))
+  if (c->cap_mode != MOE_CAP_NONE && !(c->alpha > 0.0 && isfinite(c->alpha)))
     return MOE_ERR_INVALID_ARG;
   if (c->bias_mode != MOE_BIAS_LOGIT && c->bias_mode != MOE_BIAS_SELECT) return MOE_ERR_INVALID_ARG;
   if (c->has_ffn_bias && c->act != MOE_ACT_GELU) return MOE_ERR_UNSUPPORTED;

@@ -170,34 +170,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // waiting, returns false at once, so a stalled grid costs one limit in all,
 // not one per barrier.  After false the caller must leave the kernel: the
 // counters no longer describe the grid.
+//
+// The arrival counter only grows: the arrival that returns a value in
+// [m G, (m+1) G) belongs to the m-th barrier of the launch, which is passed
+// once the counter reaches (m+1) G.  No CTA resets anything, so the last one
+// in adds nothing to the latency of the others.
 __device__ inline bool grid_barrier(GridBarrier* b, int* status, uint64_t limit_ns = kWaitLimitNs) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
-    volatile unsigned* gen = &b->gen;
+    volatile unsigned* count = &b->count;
     volatile int* abort_flag = &b->abort;
     if (*abort_flag) {
       ok = 0;
     } else {
-      const unsigned g = *gen;
       __threadfence();
       const unsigned arrived = atomicAdd(&b->count, 1u);
-      if (arrived == gridDim.x - 1) {
-        atomicExch(&b->count, 0u);
-        __threadfence();
-        atomicAdd(&b->gen, 1u);
-      } else {
-        const uint64_t t0 = globaltimer_ns();
-        while (*gen == g) {
-          if (*abort_flag) { ok = 0; break; }
-          __nanosleep(64);
-          if (globaltimer_ns() - t0 > limit_ns) {
-            set_status(status, kDevTimeout);
-            atomicExch(&b->abort, 1);
-            ok = 0;
-            break;
-          }
+      const unsigned target = (arrived / gridDim.x + 1u) * gridDim.x;
+      const uint64_t t0 = globaltimer_ns();
+      while ((int)(*count - target) < 0) {
+        if (*abort_flag) { ok = 0; break; }
+        __nanosleep(32);
+        if (globaltimer_ns() - t0 > limit_ns) {
+          set_status(status, kDevTimeout);
+          atomicExch(&b->abort, 1);
+          ok = 0;
+          break;
         }
       }
     }

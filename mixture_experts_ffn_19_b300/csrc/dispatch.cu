@@ -43,6 +43,7 @@ constexpr int kPlanThreads = 1024;
 constexpr int kPendingMark = -2;
 constexpr int kRrThreads = 128;     // reroute CTA = one chunk of 128 pending tokens
 constexpr int kRrWords = kRrThreads / 32;
+constexpr int kFusedScanInts = 16384;   // per-chunk count table summed by every reroute CTA
 
 __device__ __forceinline__ bool valid_expert(int e, int E) { return e >= 0 && e < E; }
 
@@ -61,6 +62,25 @@ __device__ int warp_exclusive_scan_column(int32_t* m, int n, int E, int e, int l
       if (lane >= o) incl += y;
     }
     if (r < n) m[(size_t)r * E + e] = carry + incl - v;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return carry;
+}
+
+// In-place exclusive scan of a contiguous int row by one warp; returns the
+// row total.  Loads go through L2, as in the column scan.
+__device__ int warp_exclusive_scan_row(int32_t* m, int n, int lane) {
+  int carry = 0;
+  for (int r0 = 0; r0 < n; r0 += 32) {
+    const int r = r0 + lane;
+    const int v = r < n ? __ldcg(&m[r]) : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (r < n) m[r] = carry + incl - v;
     carry += __shfl_sync(0xffffffffu, incl, 31);
   }
   return carry;
@@ -170,7 +190,6 @@ __global__ void __launch_bounds__(kPlanThreads) dispatch_plan_kernel(DispatchPar
     for (int w = 0; w < kPlanThreads / 32; ++w) s += warp_tot[w];
     p.rr->primary_kept = s;
     p.rr->bar.count = 0;
-    p.rr->bar.gen = 0;
     p.rr->bar.abort = 0;
   }
   for (int r = tid; r < kMaxRounds; r += kPlanThreads) p.rr->any_prop[r] = 0;
@@ -183,9 +202,19 @@ __global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchPa
   __shared__ uint32_t bits[kMaxExperts * kRrWords];
   __shared__ float prob_s[kRrThreads][TE + 1];
   __shared__ unsigned long long full_m[kMaxExperts / 64];   // bit e: expert e was full at round start
-  __shared__ int fill_s[kMaxExperts];
-  const int tid = threadIdx.x;
+  __shared__ int fill_s[kMaxExperts];            // fill levels at the start of the round
+  __shared__ int pre_s[kMaxExperts], tot_s[kMaxExperts];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int nch = (N + kRrThreads - 1) / kRrThreads;
+  // With one chunk per CTA, the chunk's staged probabilities (E <= TE) and its
+  // tokens' held experts stay on chip from round to round.
+  const bool own_one = nch <= (int)gridDim.x;
+  // While the per-chunk count table is small, every CTA sums it itself: the
+  // per-expert scan folds into the acceptance phase and a round needs one grid
+  // barrier instead of two.  The table is then double-buffered by round
+  // parity, so a CTA already proposing in the next round never overwrites
+  // counts another CTA is still summing.
+  const bool fused = (size_t)nch * E <= (size_t)kFusedScanInts;
 
   // primary decisions: an assignment keeps its expert if its rank in token
   // order (chunk base + rank inside the chunk) is below C, else it is pending
@@ -201,31 +230,40 @@ __global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchPa
       else { p.final_idx[a] = kPendingMark; p.slot[a] = -1; }
     }
   }
+  if (fused) {
+    for (int e = tid; e < E; e += kRrThreads) fill_s[e] = __ldcg(&rr->fill[0][e]);
+  }
 
-  int cur = 0;                                   // fill[cur] = levels at the start of the round
+  int cur = 0;                                   // (two barriers a round) rr->fill[cur]: start levels
+  int tile_chunk = -1;                           // chunk whose probabilities are in prob_s (E <= TE)
+  // held / prop / prank stay in registers: every index below is a
+  // compile-time constant after unrolling (slots past k are guarded); with one
+  // chunk per CTA they carry from phase A to phase C and on to the next round
+  int held[kMaxTopk], prop[kMaxTopk], prank[kMaxTopk];
   for (int round = 0;; ++round) {
     if (round >= kMaxRounds || round > E + 1) { set_status(p.status, kDevBadState); break; }
+    int32_t* cnt = p.rr_chunk + (fused ? (size_t)(round & 1) * nch * E : 0);
     // ---- phase A: proposals, per-chunk bitmap ranks and counts
+    if (!fused) {
+      __syncthreads();
+      for (int e = tid; e < E; e += kRrThreads) fill_s[e] = __ldcg(&rr->fill[cur][e]);
+    }
     for (int w = tid; w < kMaxExperts / 64; w += kRrThreads) full_m[w] = 0ull;
     __syncthreads();
     for (int e = tid; e < E; e += kRrThreads)
-      if (__ldcg(&rr->fill[cur][e]) >= C) atomicOr(&full_m[e >> 6], 1ull << (e & 63));
+      if (fill_s[e] >= C) atomicOr(&full_m[e >> 6], 1ull << (e & 63));
     __syncthreads();
     for (int c = blockIdx.x; c < nch; c += gridDim.x) {
       for (int i = tid; i < E * kRrWords; i += kRrThreads) bits[i] = 0;
       const int t = c * kRrThreads + tid;
-      // held / prop stay in registers: every index below is a compile-time
-      // constant after unrolling (slots past k are guarded)
-      int held[kMaxTopk], prop[kMaxTopk];
       bool mine = false;
 #pragma unroll
       for (int j = 0; j < kMaxTopk; ++j) {
-        held[j] = (j < k && t < N) ? p.final_idx[(size_t)t * k + j] : -1;
+        if (!own_one || round == 0) held[j] = (j < k && t < N) ? p.final_idx[(size_t)t * k + j] : -1;
         prop[j] = -1;
         mine |= held[j] == kPendingMark;
       }
       bool any = false;
-      bool tile_valid = false;                   // E <= TE: one staged tile serves every slot
       if (__syncthreads_or(mine)) {
 #pragma unroll
         for (int j = 0; j < kMaxTopk; ++j) {
@@ -235,8 +273,8 @@ __global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchPa
           float bp = -1.f;
           int be = -1;
           for (int e0 = 0; e0 < E; e0 += TE) {
-            if (E > TE || !tile_valid) {
-              tile_valid = true;
+            if (E > TE || tile_chunk != c) {
+              tile_chunk = E > TE ? -1 : c;
               // stage probabilities [tokens of the chunk][e0, e0+TE): coalesced,
               // 16 independent loads in flight per thread
               __syncthreads();
@@ -268,21 +306,47 @@ __global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchPa
                 if (jj < j && ep >= 0 && ep < TE) excl |= 1ull << ep;
               }
               const int ncol = min(TE, E - e0);
-              for (int col = 0; col < ncol; ++col) {
-                if ((excl >> col) & 1ull) continue;
+              // four independent arg-max chains over interleaved columns,
+              // merged at the end: better() is a total order (higher p, then
+              // lower index), so the winner does not depend on the grouping.
+              // The test is evaluated without short-circuits and applied as a
+              // select, so lanes never branch apart column by column.
+              float qp[4] = {bp, -1.f, -1.f, -1.f};
+              int qe[4] = {be, -1, -1, -1};
+#pragma unroll
+              for (int col = 0; col < TE; ++col) {
                 const float pe = prob_s[tid][col];
-                const int e = e0 + col;
-                if (be < 0 || better(pe, e, bp, be)) { bp = pe; be = e; }
+                const int e = e0 + col, q = col & 3;
+                const bool take = (col < ncol) & !((excl >> col) & 1ull) &
+                                  ((qe[q] < 0) | (pe > qp[q]) | ((pe == qp[q]) & (e < qe[q])));
+                qp[q] = take ? pe : qp[q];
+                qe[q] = take ? e : qe[q];
               }
+#pragma unroll
+              for (int q = 1; q < 4; ++q)
+                if (qe[q] >= 0 && (qe[0] < 0 || better(qp[q], qe[q], qp[0], qe[0]))) {
+                  qp[0] = qp[q];
+                  qe[0] = qe[q];
+                }
+              bp = qp[0];
+              be = qe[0];
             }
           }
           if (need) {
             prop[j] = be;
             if (be < 0) {
               p.final_idx[(size_t)t * k + j] = -1;        // nothing left: dropped
+              held[j] = -1;
             } else {
-              atomicOr(&bits[be * kRrWords + (tid >> 5)], 1u << (tid & 31));
               any = true;
+            }
+          }
+          // lanes proposing the same expert set their bits with one atomic
+          {
+            const unsigned act = __ballot_sync(0xffffffffu, need && be >= 0);
+            if (need && be >= 0) {
+              const unsigned same = __match_any_sync(act, be);
+              if ((tid & 31) == __ffs(same) - 1) atomicOr(&bits[be * kRrWords + (tid >> 5)], same);
             }
           }
         }
@@ -299,52 +363,95 @@ __global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchPa
             for (int w = 0; w < (tid >> 5); ++w) r += __popc(bits[e * kRrWords + w]);
             r += __popc(bits[e * kRrWords + (tid >> 5)] & lanemask_lt());
           }
-          p.rr_prop[(size_t)t * k + j] = e;
-          p.rr_rank[(size_t)t * k + j] = r;
+          prank[j] = r;
+          if (!own_one) {
+            p.rr_prop[(size_t)t * k + j] = e;
+            p.rr_rank[(size_t)t * k + j] = r;
+          }
         }
       }
       for (int e = tid; e < E; e += kRrThreads) {
         int n = 0;
         for (int w = 0; w < kRrWords; ++w) n += __popc(bits[e * kRrWords + w]);
-        p.rr_chunk[(size_t)c * E + e] = n;
+        cnt[(size_t)e * nch + c] = n;
       }
-      if (__syncthreads_or(any) && tid == 0) atomicExch(&rr->any_prop[round], 1);
+      // every CTA that proposed stores the same 1; the grid barrier publishes it
+      if (__syncthreads_or(any) && tid == 0) *(volatile int*)&rr->any_prop[round] = 1;
     }
     // a barrier that timed out (status recorded) ends the kernel for every CTA
     if (!grid_barrier(&rr->bar, p.status)) return;
     if (!__ldcg(&rr->any_prop[round])) break;    // nothing proposed: every slot is placed or dropped
-    // ---- phase B: per-expert exclusive scan over chunks (a warp per expert),
-    //      next fill levels
-    {
-      const int lane = tid & 31;
+    if (!fused) {
+      // ---- phase B: per-expert exclusive scan over chunks (a warp per
+      //      expert), next fill levels
       const int nwarps = gridDim.x * (kRrThreads / 32);
-      for (int e = blockIdx.x * (kRrThreads / 32) + (tid >> 5); e < E; e += nwarps) {
-        const int carry = warp_exclusive_scan_column(p.rr_chunk, nch, E, e, lane);
+      for (int e = blockIdx.x * (kRrThreads / 32) + wid; e < E; e += nwarps) {
+        const int carry = warp_exclusive_scan_row(cnt + (size_t)e * nch, nch, lane);
         if (lane == 0) rr->fill[cur ^ 1][e] = min(C, __ldcg(&rr->fill[cur][e]) + carry);
       }
+      if (!grid_barrier(&rr->bar, p.status)) return;
     }
-    if (!grid_barrier(&rr->bar, p.status)) return;
     // ---- phase C: acceptance in token order while the expert has room
-    for (int e = tid; e < E; e += kRrThreads) fill_s[e] = __ldcg(&rr->fill[cur][e]);
-    __syncthreads();
     for (int c = blockIdx.x; c < nch; c += gridDim.x) {
-      const int t = c * kRrThreads + tid;
-      if (t >= N) continue;
-      for (int j = 0; j < k; ++j) {
-        const size_t a = (size_t)t * k + j;
-        if (p.final_idx[a] != kPendingMark) continue;
-        const int e = p.rr_prop[a];
-        const int s = fill_s[e] + __ldcg(&p.rr_chunk[(size_t)c * E + e]) + p.rr_rank[a];
-        if (s < C) { p.final_idx[a] = e; p.slot[a] = s; }
+      if (fused) {
+        // this chunk's base per expert (proposals in earlier chunks) and the
+        // round's totals: a warp takes 8 experts at a time, its lanes stride
+        // over the chunks (the table is [expert][chunk], so loads coalesce),
+        // 8 x 4 loads in flight per lane; integer sums reduced by the warp.
+        constexpr int EB = 8;
+        for (int e0 = wid * EB; e0 < E; e0 += EB * (kRrThreads / 32)) {
+          int tot[EB], pre[EB];
+#pragma unroll
+          for (int b = 0; b < EB; ++b) tot[b] = pre[b] = 0;
+#pragma unroll 4
+          for (int c2 = lane; c2 < nch; c2 += 32) {
+#pragma unroll
+            for (int b = 0; b < EB; ++b) {
+              const int v = e0 + b < E ? __ldcg(&cnt[(size_t)(e0 + b) * nch + c2]) : 0;
+              tot[b] += v;
+              pre[b] += c2 < c ? v : 0;
+            }
+          }
+#pragma unroll
+          for (int b = 0; b < EB; ++b) {
+            const int tt = __reduce_add_sync(0xffffffffu, tot[b]);
+            const int pp = __reduce_add_sync(0xffffffffu, pre[b]);
+            if (lane == 0 && e0 + b < E) { tot_s[e0 + b] = tt; pre_s[e0 + b] = pp; }
+          }
+        }
+        __syncthreads();
       }
+      const int t = c * kRrThreads + tid;
+      if (t < N) {
+#pragma unroll
+        for (int j = 0; j < kMaxTopk; ++j) {
+          if (j >= k) break;
+          const size_t a = (size_t)t * k + j;
+          if (held[j] != kPendingMark && own_one) continue;
+          if (!own_one && p.final_idx[a] != kPendingMark) continue;
+          const int e = own_one ? prop[j] : p.rr_prop[a];
+          const int base = fused ? pre_s[e] : __ldcg(&cnt[(size_t)e * nch + c]);
+          const int s = fill_s[e] + base + (own_one ? prank[j] : p.rr_rank[a]);
+          if (s < C) {
+            p.final_idx[a] = e;
+            p.slot[a] = s;
+            held[j] = e;
+          }
+        }
+      }
+      __syncthreads();
     }
-    __syncthreads();
+    if (fused) {
+      for (int e = tid; e < E; e += kRrThreads) fill_s[e] = min(C, fill_s[e] + tot_s[e]);
+    }
     cur ^= 1;
   }
   // ---- layout from the final fill levels (CTA 0)
   if (blockIdx.x == 0) {
     __shared__ int s_kept;
-    for (int e = tid; e < E; e += kRrThreads) fill_s[e] = __ldcg(&rr->fill[cur][e]);
+    __syncthreads();
+    if (!fused)
+      for (int e = tid; e < E; e += kRrThreads) fill_s[e] = __ldcg(&rr->fill[cur][e]);
     __syncthreads();
     if (tid == 0) {
       int kept = 0;
@@ -495,7 +602,7 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(DispatchP
 
 size_t reroute_scratch_ints(int N, int k, int E) {
   const size_t chunks = (size_t)(N + kRrThreads - 1) / kRrThreads;
-  return 2 * (size_t)N * k + chunks * E;
+  return 2 * (size_t)N * k + 2 * chunks * E;   // rr_prop, rr_rank, two count tables
 }
 
 cudaError_t launch_dispatch(const DispatchParams& p, bool bf16, cudaStream_t s) {

@@ -110,7 +110,7 @@ struct DispatchParams {
   RerouteState* rr;          // reroute state (workspace)
   int32_t* rr_prop;          // [N, k] proposal of each pending slot in the round
   int32_t* rr_rank;          // [N, k] rank of each proposal inside its 128-token chunk
-  int32_t* rr_chunk;         // [ceil(N/128), E] per-chunk proposal counts, then bases
+  int32_t* rr_chunk;         // 2 x [E, ceil(N/128)] proposal counts per chunk (then bases)
   int32_t* counts;           // [E] nullable
   int32_t* n_dropped;        // nullable
   int32_t* n_rerouted;       // nullable

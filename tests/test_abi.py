@@ -79,6 +79,18 @@ def test_capacity_matches_oracle(lib, name):
     assert moe.moe_capacity(c2) == 1
 
 
+@pytest.mark.parametrize("alpha", [0.7, 0.3, 0.6, 1.1, 1.3, 0.9, 2.2, 1.25, 4.0])
+def test_capacity_factor_is_taken_exactly(lib, alpha):
+    # factors with no exact binary form, where floor(k N / E) * alpha is an
+    # integer: 1250 * 0.7 = 875, 1000 * 0.3 = 300, ...  A single-precision
+    # factor (0.7 -> 0.69999999) would floor one lower than the oracle
+    for n, e, k in [(40000, 64, 2), (16000, 32, 2), (5000, 10, 2), (100, 10, 1), (6400, 64, 8)]:
+        c = moe.make_config(n, 64, e, k, 64, cap_mode=moe.MOE_CAP_REROUTE, alpha=alpha)
+        assert moe.moe_capacity(c) == oracle.capacity(n, e, k, alpha), (n, e, k, alpha)
+    c = moe.make_config(40000, 64, 64, 2, 64, cap_mode=moe.MOE_CAP_DROP, alpha=0.7)
+    assert moe.moe_capacity(c) == 875
+
+
 def test_sizes(lib):
     w = synth.WORKLOADS["dsv2"]
     c = config_of(w)

@@ -98,6 +98,12 @@ CASES = [
     # reroute ranked by p + b (selection-only bias)
     synth.small_workload("e64_reroute", n_tokens=1500, d_model=64, alpha=0.7,
                          bias_law=synth.BIAS_UNIFORM_P, bias_mode=1),
+    # the reroute kernel's other paths: a per-chunk count table too large for
+    # every CTA to sum (71 chunks x 256 experts), more 128-token chunks than
+    # co-resident CTAs (313), and both at once
+    synth.small_workload("e64_reroute", n_tokens=9000, d_model=64, n_experts=256, alpha=0.5),
+    synth.small_workload("e64_reroute", n_tokens=40000, d_model=64, n_experts=32, alpha=0.5),
+    synth.small_workload("e64_reroute", n_tokens=40000, d_model=64, n_experts=64, alpha=0.7),
 ]
 
 
