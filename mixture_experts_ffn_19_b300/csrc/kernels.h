@@ -75,8 +75,8 @@ struct RouteSplit {
   int ks, k_slice;
 };
 RouteSplit route_split(int N, int d, bool bf16);
-int route_finish_blocks(int N);
-__host__ __device__ int route_finish_tpw(int N);
+int route_finish_blocks(int N, int gw);
+__host__ __device__ int route_finish_iters(int N, int gw);
 cudaError_t launch_route_logits_tc(const RouteSplit& s, const void* x, const void* w_router,
                                    int N, int E, int d, float* part, int* status,
                                    cudaStream_t stream);

@@ -120,17 +120,34 @@ __global__ void __launch_bounds__(kThreads) route_logits_simt(RouteParams p, Rou
   }
 }
 
-// Warp per token: logits from the partials, bias, softmax, top-k, gates.
-template <int EJ>
+// G lanes per token (G = 8, 16 or 32, so that each lane holds EJ <= 8
+// experts): logits from the partials, bias, softmax, top-k, gates.  A warp
+// works on 32 / G tokens at once; the reductions over a token's experts are
+// shuffles within its G-lane group.
+template <int G>
+__device__ __forceinline__ float group_max(float v) {
+#pragma unroll
+  for (int o = G / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+template <int G>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <int EJ, int G>
 __global__ void __launch_bounds__(kThreads) route_finish_kernel(RouteParams p, RouteSplit sp) {
   griddep_begin();
-  constexpr int EP = EJ * 32;
+  constexpr int EP = EJ * G, GW = 32 / G;
   __shared__ unsigned long long psum_w[kWarps][EP];
   __shared__ unsigned long long zh_w[kWarps][2];
   __shared__ int picks_s[EP];
   __shared__ bool last_cta;
   const int E = p.E, N = p.N, k = p.k;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int sub = lane % G, grp = lane / G, base = grp * G;   // lane in the token's group
   // bias on the logits (before the softmax) or on the selection key only
   const bool bias_logit = p.bias && !p.bias_select, bias_sel = p.bias && p.bias_select;
   for (int e = tid; e < EP; e += kThreads) picks_s[e] = 0;
@@ -138,26 +155,29 @@ __global__ void __launch_bounds__(kThreads) route_finish_kernel(RouteParams p, R
   unsigned long long psum[EJ];                  // sum of p in units of 2^-40 (exact)
 #pragma unroll
   for (int c = 0; c < EJ; ++c) psum[c] = 0ull;
-  unsigned long long zacc = 0ull, hacc = 0ull;  // lane 0: lse^2 (2^-20), H (2^-40)
+  unsigned long long zacc = 0ull, hacc = 0ull;  // group lane 0: lse^2 (2^-20), H (2^-40)
   float b[EJ];                                  // this lane's bias values
 #pragma unroll
   for (int c = 0; c < EJ; ++c) {
-    const int e = lane + 32 * c;
+    const int e = sub + G * c;
     b[c] = (p.bias && e < E) ? p.bias[e] : 0.f;
   }
-  const int tpw = route_finish_tpw(N);
-  for (int i = 0; i < tpw; ++i) {
-    const int t = (blockIdx.x * kWarps + warp) * tpw + i;
-    if (t >= N) break;
+  const int iters = route_finish_iters(N, GW);
+  for (int i = 0; i < iters; ++i) {
+    const int t_first = ((blockIdx.x * kWarps + warp) * iters + i) * GW;
+    if (t_first >= N) break;                    // the whole warp leaves together
+    const int t = t_first + grp;
+    const bool valid = t < N;                   // groups past N compute on zeros, write nothing
     float v[EJ], raw[EJ];
     float m = -INFINITY, mr = -INFINITY;
     // logits: the K-slice partials summed in slice order (compensated fp32)
 #pragma unroll
     for (int c = 0; c < EJ; ++c) {
-      const int e = lane + 32 * c;
+      const int e = sub + G * c;
       if (e < E) {
         KahanF z;
-        for (int s0 = 0; s0 < sp.ks; ++s0) z.add(p.part[((size_t)s0 * N + t) * E + e]);
+        if (valid)
+          for (int s0 = 0; s0 < sp.ks; ++s0) z.add(p.part[((size_t)s0 * N + t) * E + e]);
         raw[c] = z.s;
       } else {
         raw[c] = -INFINITY;
@@ -166,35 +186,35 @@ __global__ void __launch_bounds__(kThreads) route_finish_kernel(RouteParams p, R
       m = fmaxf(m, v[c]);
       mr = fmaxf(mr, raw[c]);
     }
-    m = warp_max(m);
+    m = group_max<G>(m);
     float s = 0.f;
 #pragma unroll
     for (int c = 0; c < EJ; ++c) {
-      v[c] = (lane + 32 * c < E) ? expf(v[c] - m) : 0.f;
+      v[c] = (sub + G * c < E) ? expf(v[c] - m) : 0.f;
       s += v[c];
     }
-    s = warp_sum(s);
+    s = group_sum<G>(s);
     if (p.z_loss) {
       // logsumexp of the bias-free logits («项目概述：为什么MoE...» §3.3)
       float lse;
       if (bias_logit) {
-        mr = warp_max(mr);
+        mr = group_max<G>(mr);
         float sr = 0.f;
 #pragma unroll
-        for (int c = 0; c < EJ; ++c) sr += (lane + 32 * c < E) ? expf(raw[c] - mr) : 0.f;
-        lse = mr + logf(warp_sum(sr));
+        for (int c = 0; c < EJ; ++c) sr += (sub + G * c < E) ? expf(raw[c] - mr) : 0.f;
+        lse = mr + logf(group_sum<G>(sr));
       } else {
         lse = m + logf(s);
       }
-      if (lane == 0) zacc += __float2ull_rn(lse * lse * 1048576.0f);
+      if (sub == 0 && valid) zacc += __float2ull_rn(lse * lse * 1048576.0f);
     }
     float key[EJ];   // what the top-k ranks: p, or p + b under selection-only bias
 #pragma unroll
     for (int c = 0; c < EJ; ++c) {
-      const int e = lane + 32 * c;
+      const int e = sub + G * c;
       v[c] = v[c] / s;
       key[c] = bias_sel ? v[c] + b[c] : v[c];
-      if (e < E) {
+      if (e < E && valid) {
         psum[c] += __float2ull_rn(v[c] * 1099511627776.0f);
         if (p.probs) p.probs[(size_t)t * E + e] = key[c];
       }
@@ -207,11 +227,11 @@ __global__ void __launch_bounds__(kThreads) route_finish_kernel(RouteParams p, R
       int be = 0x7fffffff;
 #pragma unroll
       for (int c = 0; c < EJ; ++c) {
-        const int e = lane + 32 * c;
+        const int e = sub + G * c;
         if (e < E && !((taken >> c) & 1u) && better(key[c], e, bk, be)) { bk = key[c]; be = e; }
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
+      for (int o = G / 2; o > 0; o >>= 1) {
         const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
         const int oe = __shfl_xor_sync(0xffffffffu, be, o);
         if (better(ok, oe, bk, be)) { bk = ok; be = oe; }
@@ -222,27 +242,38 @@ __global__ void __launch_bounds__(kThreads) route_finish_kernel(RouteParams p, R
         float mine = 0.f;
 #pragma unroll
         for (int c = 0; c < EJ; ++c)
-          if (c == (be >> 5)) mine = v[c];
-        pw = __shfl_sync(0xffffffffu, mine, be & 31);
+          if (c == be / G) mine = v[c];
+        pw = __shfl_sync(0xffffffffu, mine, base + be % G);
       }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (q == lane) { my_p = pw; my_e = be; }
+      if (be % G == sub) taken |= 1u << (be / G);
+      if (q == sub) { my_p = pw; my_e = be; }
       ksum += pw;
     }
     const float my_w = my_p / ksum;
-    if (lane < k) {
-      p.topk_idx[(size_t)t * k + lane] = my_e;
-      p.topk_w[(size_t)t * k + lane] = my_w;
+    if (sub < k && valid) {
+      p.topk_idx[(size_t)t * k + sub] = my_e;
+      p.topk_w[(size_t)t * k + sub] = my_w;
       atomicAdd(&picks_s[my_e], 1);
     }
     if (p.entropy) {
       // -sum_j w_j log2 w_j over the gates («GPT-4 Has 1.8 Trillion ...» §2.3)
-      const float h = warp_sum((lane < k && my_w > 0.f) ? -my_w * log2f(my_w) : 0.f);
-      if (lane == 0) hacc += __float2ull_rn(h * 1099511627776.0f);
+      const float h = group_sum<G>((sub < k && my_w > 0.f) ? -my_w * log2f(my_w) : 0.f);
+      if (sub == 0 && valid) hacc += __float2ull_rn(h * 1099511627776.0f);
     }
   }
+  // the groups of a warp hold partial sums of the same experts: add them
+  // (integers, so the order does not matter)
 #pragma unroll
-  for (int c = 0; c < EJ; ++c) psum_w[warp][lane + 32 * c] = psum[c];
+  for (int o = G; o < 32; o <<= 1) {
+#pragma unroll
+    for (int c = 0; c < EJ; ++c) psum[c] += __shfl_xor_sync(0xffffffffu, psum[c], o);
+    zacc += __shfl_xor_sync(0xffffffffu, zacc, o);
+    hacc += __shfl_xor_sync(0xffffffffu, hacc, o);
+  }
+  if (grp == 0) {
+#pragma unroll
+    for (int c = 0; c < EJ; ++c) psum_w[warp][sub + G * c] = psum[c];
+  }
   if (lane == 0) { zh_w[warp][0] = zacc; zh_w[warp][1] = hacc; }
   __syncthreads();
   // integer sums are exact, so the cross-CTA atomics are order-independent
@@ -307,13 +338,43 @@ cudaError_t launch_simt_t(const RouteParams& p, const RouteSplit& sp, cudaStream
   return cudaSuccess;
 }
 
-template <int EJ>
+template <int EJ, int G>
 cudaError_t launch_finish_t(const RouteParams& p, const RouteSplit& sp, cudaStream_t s) {
-  const cudaError_t err =
-      launch_chained(route_finish_kernel<EJ>, route_finish_blocks(p.N), kThreads, 0, s, p, sp);
+  const cudaError_t err = launch_chained(route_finish_kernel<EJ, G>, route_finish_blocks(p.N, 32 / G),
+                                         kThreads, 0, s, p, sp);
   if (err != cudaSuccess) return err;
   count_launch();
   return cudaSuccess;
+}
+
+// lanes per token: the fewest of 8, 16, 32 that keep a lane at <= 8 experts
+cudaError_t launch_finish(const RouteParams& p, const RouteSplit& sp, cudaStream_t s) {
+  if (p.E <= 64) {
+    switch ((p.E + 7) / 8) {
+      case 1: return launch_finish_t<1, 8>(p, sp, s);
+      case 2: return launch_finish_t<2, 8>(p, sp, s);
+      case 3: return launch_finish_t<3, 8>(p, sp, s);
+      case 4: return launch_finish_t<4, 8>(p, sp, s);
+      case 5: return launch_finish_t<5, 8>(p, sp, s);
+      case 6: return launch_finish_t<6, 8>(p, sp, s);
+      case 7: return launch_finish_t<7, 8>(p, sp, s);
+      default: return launch_finish_t<8, 8>(p, sp, s);
+    }
+  }
+  if (p.E <= 128) {
+    switch ((p.E + 15) / 16) {
+      case 5: return launch_finish_t<5, 16>(p, sp, s);
+      case 6: return launch_finish_t<6, 16>(p, sp, s);
+      case 7: return launch_finish_t<7, 16>(p, sp, s);
+      default: return launch_finish_t<8, 16>(p, sp, s);
+    }
+  }
+  switch ((p.E + 31) / 32) {
+    case 5: return launch_finish_t<5, 32>(p, sp, s);
+    case 6: return launch_finish_t<6, 32>(p, sp, s);
+    case 7: return launch_finish_t<7, 32>(p, sp, s);
+    default: return launch_finish_t<8, 32>(p, sp, s);
+  }
 }
 
 #define MOE_EJ_SWITCH(E, F, ...)                  \
@@ -330,14 +391,16 @@ cudaError_t launch_finish_t(const RouteParams& p, const RouteSplit& sp, cudaStre
 
 }  // namespace
 
-// Tokens per finish warp: one for small batches (latency), up to 8 for large ones.
-__host__ __device__ int route_finish_tpw(int N) {
-  const int t = N / (148 * kWarps * 2);
-  return t < 1 ? 1 : (t > 8 ? 8 : t);
+// Tokens per finish warp: one for small batches (latency), up to 8 for large
+// ones; a warp takes gw tokens per iteration.
+__host__ __device__ int route_finish_iters(int N, int gw) {
+  int t = N / (148 * kWarps * 2);
+  t = t < 1 ? 1 : (t > 8 ? 8 : t);
+  return (t + gw - 1) / gw;
 }
 
-int route_finish_blocks(int N) {
-  const int per_cta = kWarps * route_finish_tpw(N);
+int route_finish_blocks(int N, int gw) {
+  const int per_cta = kWarps * route_finish_iters(N, gw) * gw;
   return (N + per_cta - 1) / per_cta;
 }
 
@@ -374,7 +437,7 @@ cudaError_t launch_route(const RouteParams& p, bool bf16, cudaStream_t s) {
     err = [&]() -> cudaError_t { MOE_EJ_SWITCH(p.E, launch_simt_t, p, sp, s) }();
   }
   if (err != cudaSuccess) return err;
-  MOE_EJ_SWITCH(p.E, launch_finish_t, p, sp, s)
+  return launch_finish(p, sp, s);
 }
 
 
