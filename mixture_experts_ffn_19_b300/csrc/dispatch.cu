@@ -127,27 +127,42 @@ __global__ void __launch_bounds__(kRankTC) dispatch_rank_kernel(DispatchParams p
 
 // Segment layout, counts and drop/reroute totals from the final per-expert
 // fill levels; perm = -1 on the padding rows.  Executed by one whole CTA.
-__device__ void write_layout(const DispatchParams& p, const int* fill, int n_dropped,
+// The segment starts are scanned by warp 0 into shared memory and every
+// later step reads them there: read back from global memory inside the
+// padding loop (which also stores), each expert cost an L2 round trip.
+constexpr int kLayoutInts = kMaxExperts + 8 + 1;   // routed + shared segments + end
+__device__ void write_layout(const DispatchParams& p, const int* fill, int* offs_s, int n_dropped,
                              int n_rerouted) {
   const int E = p.E, S = p.S, N = p.N;
-  if (threadIdx.x == 0) {
-    if (p.n_dropped) *p.n_dropped = n_dropped;
-    if (p.n_rerouted) *p.n_rerouted = n_rerouted;
-    int row = 0;
-    for (int e = 0; e < E; ++e) {
-      p.offsets[e] = row;
-      row += (fill[e] + kAlign - 1) / kAlign * kAlign;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (wid == 0) {
+    // exclusive scan of the 128-row-padded fills
+    int carry = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int v = e < E ? (fill[e] + kAlign - 1) / kAlign * kAlign : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (e < E) offs_s[e] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    const int nseg = (N + kAlign - 1) / kAlign * kAlign;
-    for (int s = 0; s < S; ++s) { p.offsets[E + s] = row; row += nseg; }
-    p.offsets[E + S] = row;
+    if (lane == 0) {
+      const int nseg = (N + kAlign - 1) / kAlign * kAlign;
+      for (int sh = 0; sh <= S; ++sh) offs_s[E + sh] = carry + sh * nseg;
+      if (p.n_dropped) *p.n_dropped = n_dropped;
+      if (p.n_rerouted) *p.n_rerouted = n_rerouted;
+    }
   }
-  for (int e = threadIdx.x; e < E; e += blockDim.x) if (p.counts) p.counts[e] = fill[e];
   __syncthreads();
-  const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  for (int e = threadIdx.x >> 5; e < E; e += nw) {
-    const int r0 = p.offsets[e] + fill[e];
-    const int r1 = p.offsets[e + 1];
+  for (int i = threadIdx.x; i <= E + S; i += blockDim.x) p.offsets[i] = offs_s[i];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) if (p.counts) p.counts[e] = fill[e];
+  for (int e = wid; e < E; e += nw) {
+    const int r0 = offs_s[e] + fill[e];
+    const int r1 = offs_s[e + 1];
     for (int r = r0 + lane; r < r1; r += 32) p.perm[r] = -1;
   }
 }
@@ -156,6 +171,7 @@ __global__ void __launch_bounds__(kPlanThreads) dispatch_plan_kernel(DispatchPar
   griddep_begin();
   const int E = p.E, C = p.C;
   __shared__ int fill[kMaxExperts], total[kMaxExperts];
+  __shared__ int offs_s[kLayoutInts];
   __shared__ int warp_tot[kPlanThreads / 32];
   __shared__ int s_total;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -175,7 +191,7 @@ __global__ void __launch_bounds__(kPlanThreads) dispatch_plan_kernel(DispatchPar
     __syncthreads();
     if (tid == 0) { int s = 0; for (int w = 0; w < kPlanThreads / 32; ++w) s += warp_tot[w]; s_total = s; }
     __syncthreads();
-    write_layout(p, fill, s_total, 0);
+    write_layout(p, fill, offs_s, s_total, 0);
     return;
   }
 
@@ -204,6 +220,7 @@ __global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchPa
   __shared__ unsigned long long full_m[kMaxExperts / 64];   // bit e: expert e was full at round start
   __shared__ int fill_s[kMaxExperts];            // fill levels at the start of the round
   __shared__ int pre_s[kMaxExperts], tot_s[kMaxExperts];
+  __shared__ int offs_s[kLayoutInts];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int nch = (N + kRrThreads - 1) / kRrThreads;
   // With one chunk per CTA, the chunk's staged probabilities (E <= TE) and its
@@ -459,7 +476,7 @@ __global__ void __launch_bounds__(kRrThreads) dispatch_reroute_kernel(DispatchPa
       s_kept = kept;
     }
     __syncthreads();
-    write_layout(p, fill_s, N * k - s_kept, s_kept - __ldcg(&rr->primary_kept));
+    write_layout(p, fill_s, offs_s, N * k - s_kept, s_kept - __ldcg(&rr->primary_kept));
   }
 }
 
@@ -521,7 +538,7 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(DispatchP
   griddep_wait();
   if (MOE_DISPATCH_EARLY_TRIGGER) griddep_launch_dependents();
   __shared__ int idx_s[kSmallAssign];
-  __shared__ int hist[kMaxExperts], fill[kMaxExperts], offs[kMaxExperts];
+  __shared__ int hist[kMaxExperts], fill[kMaxExperts], offs[kLayoutInts];
   __shared__ int my_e[kMaxTopk], my_rank[kMaxTopk], rows[kMaxTopk];
   __shared__ int s_dropped;
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
@@ -583,7 +600,7 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(DispatchP
     if (row >= 0) p.perm[row] = t;
     rows[tid] = row;
   }
-  if (blockIdx.x == 0) write_layout(p, fill, s_dropped, 0);   // whole CTA
+  if (blockIdx.x == 0) write_layout(p, fill, offs, s_dropped, 0);   // whole CTA
   __syncthreads();
   const int nvec = p.d * (int)sizeof(T) / 16;
   const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.x) + (size_t)t * p.d);
