@@ -44,10 +44,16 @@ struct Vec<float> {
   }
 };
 
-template <typename T>
+// VPT 16-byte vectors per thread, loaded for RG rows at a time before any
+// FMA.  With short rows and few rows per token (the 64-expert layer: 256
+// vectors, 2 rows) two vectors per thread halve the CTA, so twice the tokens,
+// and their row bytes, are in flight per SM: 53 -> 41 us there.  With long
+// rows or many rows per token (8 rows of 640 vectors) the CTA already keeps
+// enough in flight and the smaller row groups only add latency.
+template <typename T, int VPT>
 __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
   griddep_begin();
-  constexpr int VN = Vec<T>::n;
+  constexpr int VN = Vec<T>::n, RG = VPT >= 4 ? 2 : 4 / VPT;
   const int t = blockIdx.x;
   __shared__ int rows[kMaxTopk + 8];
   __shared__ float gates[kMaxTopk + 8];
@@ -74,32 +80,44 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
     if (lane == 0) nrows = __popc(kept);
   }
   __syncthreads();
-  const int nvec = p.d / VN;
+  const int nvec = p.d / VN, nt = blockDim.x;
   const uint4* src = static_cast<const uint4*>(p.y_perm);
   uint4* dst = static_cast<uint4*>(p.y);
   const int n = nrows;
-  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-    float acc[VN];
+  for (int v0 = threadIdx.x; v0 < nvec; v0 += nt * VPT) {
+    float acc[VPT][VN];
 #pragma unroll
-    for (int q = 0; q < VN; ++q) acc[q] = 0.f;
-    // rows in groups of 4: the loads of a group are issued before its FMAs
-    for (int r0 = 0; r0 < n; r0 += 4) {
-      uint4 u[4];
+    for (int b = 0; b < VPT; ++b)
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (r0 + i < n) u[i] = src[(size_t)rows[r0 + i] * nvec + v];
+      for (int q = 0; q < VN; ++q) acc[b][q] = 0.f;
+    // rows in groups of RG: the loads of a group (all VPT vectors) are issued
+    // before its FMAs
+    for (int r0 = 0; r0 < n; r0 += RG) {
+      uint4 u[RG][VPT];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < RG; ++i)
+#pragma unroll
+        for (int b = 0; b < VPT; ++b)
+          if (r0 + i < n && v0 + b * nt < nvec) u[i][b] = src[(size_t)rows[r0 + i] * nvec + v0 + b * nt];
+#pragma unroll
+      for (int i = 0; i < RG; ++i) {
         if (r0 + i < n) {
-          float f[VN];
-          Vec<T>::load(u[i], f);
           const float g = gates[r0 + i];
 #pragma unroll
-          for (int q = 0; q < VN; ++q) acc[q] = fmaf(g, f[q], acc[q]);
+          for (int b = 0; b < VPT; ++b) {
+            if (v0 + b * nt < nvec) {
+              float f[VN];
+              Vec<T>::load(u[i][b], f);
+#pragma unroll
+              for (int q = 0; q < VN; ++q) acc[b][q] = fmaf(g, f[q], acc[b][q]);
+            }
+          }
         }
       }
     }
-    dst[(size_t)t * nvec + v] = Vec<T>::store(acc);
+#pragma unroll
+    for (int b = 0; b < VPT; ++b)
+      if (v0 + b * nt < nvec) dst[(size_t)t * nvec + v0 + b * nt] = Vec<T>::store(acc[b]);
   }
 }
 
@@ -108,9 +126,16 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
 cudaError_t launch_combine(const CombineParams& p, bool bf16, cudaStream_t s) {
   const int vn = bf16 ? 8 : 4;
   const int nvec = p.d / vn;
-  int threads = nvec < 256 ? ((nvec + 31) / 32) * 32 : 256;
-  const cudaError_t err = bf16 ? launch_chained(combine_kernel<__nv_bfloat16>, p.N, threads, 0, s, p)
-                               : launch_chained(combine_kernel<float>, p.N, threads, 0, s, p);
+  const int vpt = (nvec >= 128 && nvec <= 256 && p.S + p.k <= 4) ? 2 : 1;
+  const int per = (nvec + vpt - 1) / vpt;
+  const int threads = per < 256 ? ((per + 31) / 32) * 32 : 256;
+  cudaError_t err;
+  if (vpt == 2)
+    err = bf16 ? launch_chained(combine_kernel<__nv_bfloat16, 2>, p.N, threads, 0, s, p)
+               : launch_chained(combine_kernel<float, 2>, p.N, threads, 0, s, p);
+  else
+    err = bf16 ? launch_chained(combine_kernel<__nv_bfloat16, 1>, p.N, threads, 0, s, p)
+               : launch_chained(combine_kernel<float, 1>, p.N, threads, 0, s, p);
   if (err != cudaSuccess) return err;
   count_launch();
   return cudaSuccess;

@@ -97,7 +97,18 @@ def test_expert_ffn(cuda, w, with_counts):
     print(f"{w.name}: worst per-expert rel err {worst:.3g}")
 
 
-@pytest.mark.parametrize("w", [CASES[2], CASES[5], CASES[7]], ids=lambda w: w.name)
+COMBINE_CASES = [
+    CASES[2], CASES[5], CASES[7],
+    # rows of 128-256 16-byte vectors with at most 4 per token take two
+    # vectors per thread: a full row (the 64-expert shape), a ragged one with a
+    # shared expert, and an fp32 one
+    synth.small_workload("e64_reroute", n_tokens=300, d_model=2048, alpha=1.5),
+    synth.small_workload("dsv2", n_tokens=150, d_model=1040, n_experts=12, top_k=3, n_shared=1),
+    synth.small_workload("tiny_fp32", n_tokens=120, d_model=1000, n_experts=6, top_k=2),
+]
+
+
+@pytest.mark.parametrize("w", COMBINE_CASES, ids=lambda w: f"{w.name}-d{w.d_model}")
 def test_combine(cuda, w):
     inp = synth.make_inputs(w, with_experts=False)
     r, dsp = oracle_routing(w, inp)
