@@ -31,6 +31,7 @@ struct Ctrl {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t acc_full;
+  uint64_t staged;               // the four epilogue warps have written their rows
   uint32_t tmem_base;
   int abort;
 };
@@ -63,6 +64,7 @@ route_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(&ctrl->full[s], 1); mbar_init(&ctrl->empty[s], 1); }
     mbar_init(&ctrl->acc_full, 1);
+    mbar_init(&ctrl->staged, 128);
     ctrl->abort = 0;
     fence_mbar_init();
   }
@@ -112,8 +114,13 @@ route_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     const bool ok = mbar_wait(&ctrl->acc_full, 0, abort, p.status);
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
-      const int t = t0 + q * 32 + lane;
-      float* dst = p.part + ((size_t)ks * p.N + t) * p.E;
+      // the tile's logits go through shared memory (the ring is idle once the
+      // last MMA has completed): a thread per token row writes its row there,
+      // then the four warps store the tile's contiguous rows coalesced
+      // (scattered 4-byte stores of each row cost about 4 us per tile)
+      const int ES = p.E + 1;
+      float* stage = reinterpret_cast<float*>(smem);   // [128][E + 1]
+      const int row = q * 32 + lane;
       const int used = KB < p.nacc ? KB : p.nacc;
       for (int c = 0; c < p.acc_cols / 32; ++c) {
         KahanF acc[32];
@@ -124,11 +131,24 @@ route_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
 #pragma unroll
           for (int i = 0; i < 32; ++i) acc[i].add(__uint_as_float(r[i]));
         }
-        if (t < p.N) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c * 32 + i < p.E) dst[c * 32 + i] = acc[i].s;
-        }
+        for (int i = 0; i < 32; ++i)
+          if (c * 32 + i < p.E) stage[row * ES + c * 32 + i] = acc[i].s;
+      }
+      // a bounded hand-off (an mbarrier, not a named barrier): a warp that
+      // gave up earlier cannot leave the others waiting for ever
+      mbar_arrive(&ctrl->staged);
+      const bool staged = mbar_wait(&ctrl->staged, 0, abort, p.status);
+      const int rows = staged ? min(BM, p.N - t0) : 0, n_all = rows * p.E;
+      float* dst = p.part + ((size_t)ks * p.N + t0) * p.E;
+      const int et = threadIdx.x - 64;                 // 0 .. 127
+      const int de = 128 % p.E, dr = 128 / p.E;
+      int cc = et % p.E, rr = et / p.E;
+      for (int i = et; i < n_all; i += 128) {
+        dst[i] = stage[rr * ES + cc];
+        cc += de;
+        rr += dr;
+        if (cc >= p.E) { cc -= p.E; ++rr; }
       }
     }
   }
