@@ -16,7 +16,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kBM = 64, kBN = 64, kBK = 16, kPad = 4;
+constexpr int kBM = 64, kBN = 64, kBK = 32, kPad = 4;
 
 __device__ __forceinline__ float gelu_erf(float a) {
   return 0.5f * a * (1.f + erff(a * 0.70710678118654752f));
@@ -69,23 +69,37 @@ __global__ void __launch_bounds__(256) ffn_simt_kernel(FfnParams p) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = accu[i][j] = 0.f;
 
-  const int lr = tid >> 2, lk = (tid & 3) * 4;   // loader: row, k offset (4 floats)
+  // loader: rows lr and lr + 32, k offset lk (4 floats); the next K step's
+  // tiles are loaded into registers while the current one is computed
+  const int lr = tid >> 3, lk = (tid & 7) * 4;
+  float4 ra[2], rb[2], ru[2];
+  auto load = [&](int k0) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = lr + 32 * h, ar = a_row0 + r;
+      const bool kin = k0 + lk < K;
+      ra[h] = (ar < a_rows && kin) ? *reinterpret_cast<const float4*>(A + (size_t)ar * K + k0 + lk)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      rb[h] = (n0 + r < NO && kin) ? *reinterpret_cast<const float4*>(W + (size_t)(n0 + r) * K + k0 + lk)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (SWIGLU && STAGE == 1)
+        ru[h] = (n0 + r < NO && kin) ? *reinterpret_cast<const float4*>(U + (size_t)(n0 + r) * K + k0 + lk)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  load(0);
   for (int k0 = 0; k0 < K; k0 += kBK) {
-    {
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-      const int ar = a_row0 + lr;
-      if (ar < a_rows && k0 + lk < K) a = *reinterpret_cast<const float4*>(A + (size_t)ar * K + k0 + lk);
-      As[lk + 0][lr] = a.x; As[lk + 1][lr] = a.y; As[lk + 2][lr] = a.z; As[lk + 3][lr] = a.w;
-      float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (n0 + lr < NO && k0 + lk < K) b = *reinterpret_cast<const float4*>(W + (size_t)(n0 + lr) * K + k0 + lk);
-      Bs[lk + 0][lr] = b.x; Bs[lk + 1][lr] = b.y; Bs[lk + 2][lr] = b.z; Bs[lk + 3][lr] = b.w;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = lr + 32 * h;
+      As[lk + 0][r] = ra[h].x; As[lk + 1][r] = ra[h].y; As[lk + 2][r] = ra[h].z; As[lk + 3][r] = ra[h].w;
+      Bs[lk + 0][r] = rb[h].x; Bs[lk + 1][r] = rb[h].y; Bs[lk + 2][r] = rb[h].z; Bs[lk + 3][r] = rb[h].w;
       if (SWIGLU && STAGE == 1) {
-        float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (n0 + lr < NO && k0 + lk < K) u = *reinterpret_cast<const float4*>(U + (size_t)(n0 + lr) * K + k0 + lk);
-        Us[lk + 0][lr] = u.x; Us[lk + 1][lr] = u.y; Us[lk + 2][lr] = u.z; Us[lk + 3][lr] = u.w;
+        Us[lk + 0][r] = ru[h].x; Us[lk + 1][r] = ru[h].y; Us[lk + 2][r] = ru[h].z; Us[lk + 3][r] = ru[h].w;
       }
     }
     __syncthreads();
+    if (k0 + kBK < K) load(k0 + kBK);
 #pragma unroll
     for (int kk = 0; kk < kBK; ++kk) {
       const float4 a = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
