@@ -39,7 +39,7 @@ Layout layout_of(const moe_config* c) {
   Layout L;
   const size_t N = (size_t)c->n_tokens, k = (size_t)c->top_k, E = (size_t)c->n_experts;
   const size_t es = c->dtype == MOE_BF16 ? 2 : 4;
-  const RouteSplit rs = route_split(c->n_tokens, c->d_model, c->dtype == MOE_BF16);
+  const RouteSplit rs = route_split(c->n_tokens, c->d_model, c->n_experts, c->dtype == MOE_BF16);
   const size_t chunks = (N + kRankTC - 1) / kRankTC;
   size_t off = 0;
   auto take = [&](size_t bytes) { const size_t o = off; off = align_up(off + bytes, kWsAlign); return o; };

@@ -74,7 +74,7 @@ cudaError_t launch_bias_update(const int* picks, float* bias, int N, int E, int 
 struct RouteSplit {
   int ks, k_slice;
 };
-RouteSplit route_split(int N, int d, bool bf16);
+RouteSplit route_split(int N, int d, int E, bool bf16);
 int route_finish_blocks(int N, int gw);
 __host__ __device__ int route_finish_iters(int N, int gw);
 cudaError_t launch_route_logits_tc(const RouteSplit& s, const void* x, const void* w_router,
