@@ -391,12 +391,14 @@ cudaError_t launch_finish(const RouteParams& p, const RouteSplit& sp, cudaStream
 
 }  // namespace
 
-// Tokens per finish warp: one for small batches (latency), up to 8 for large
-// ones; a warp takes gw tokens per iteration.
+// Iterations of a finish warp: one (its gw tokens), whatever N.  The kernel is
+// a latency chain per token, so more CTAs beat more tokens per warp: with up
+// to 8 tokens per warp for large batches the 64-expert route stage took
+// 57.7 us, with one iteration 45.6 us (DeepSeek-V2 87.7 -> 81.0 us).
 __host__ __device__ int route_finish_iters(int N, int gw) {
-  int t = N / (148 * kWarps * 2);
-  t = t < 1 ? 1 : (t > 8 ? 8 : t);
-  return (t + gw - 1) / gw;
+  (void)N;
+  (void)gw;
+  return 1;
 }
 
 int route_finish_blocks(int N, int gw) {
