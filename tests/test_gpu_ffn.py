@@ -105,6 +105,9 @@ COMBINE_CASES = [
     synth.small_workload("e64_reroute", n_tokens=300, d_model=2048, alpha=1.5),
     synth.small_workload("dsv2", n_tokens=150, d_model=1040, n_experts=12, top_k=3, n_shared=1),
     synth.small_workload("tiny_fp32", n_tokens=120, d_model=1000, n_experts=6, top_k=2),
+    # fewer than 1024 tokens with rows wider than one CTA pass: several CTAs
+    # per token, each over its own range of the row (3 here, the last ragged)
+    synth.small_workload("dsv2", n_tokens=64, d_model=5136, n_experts=24, top_k=6, n_shared=2),
 ]
 
 
