@@ -77,6 +77,15 @@ SMALL = [
     # selection-only bias (DeepSeek-V3 style), fp32 and bf16
     synth.small_workload("dsv2_select", n_tokens=700, d_model=256, n_experts=64, top_k=6),
     synth.small_workload("tiny_fp32", n_tokens=150, bias_law=synth.BIAS_UNIFORM_P, bias_mode=1),
+    # each lane-group width of the finish kernel: 8 lanes per token up to 64
+    # experts (above), 16 up to 128, 32 beyond; the upper bounds of each, a
+    # ragged group, both dtypes, selection-only bias, and a batch large enough
+    # for many CTAs of 8-token warps
+    synth.small_workload("dsv2", n_tokens=333, d_model=256, n_experts=65, top_k=6),
+    synth.small_workload("dsv2", n_tokens=2500, d_model=128, n_experts=100, top_k=4),
+    synth.small_workload("dsv2_select", n_tokens=400, d_model=128, n_experts=128, top_k=8),
+    synth.small_workload("tiny_fp32", n_tokens=300, n_experts=97, top_k=5),
+    synth.small_workload("dsv2", n_tokens=600, d_model=128, n_experts=200, top_k=6),
 ]
 
 
