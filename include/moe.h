@@ -263,8 +263,13 @@ int moe_router_bias_update(const moe_config* cfg, const void* workspace, size_t 
  * Trillion Parameters...» §4.4: expert weights in low precision with
  * per-expert scales, router kept in high precision.  Format: OCP FP8 E4M3
  * (bias 7, 3 mantissa bits, subnormals, largest finite 448, no infinities).
- * Weights only: activations stay bf16, accumulation fp32, H is bf16 as in the
- * bf16 layer.  The dequantised weight is scale * value(code). */
+ * Weights only: the dequantised weight is scale * value(code); accumulation
+ * is fp32.  The tensor cores take the codes widened to f16 (exact) times f16
+ * copies of the bf16 token rows (exact from 2^-14 to 65504; smaller values
+ * round to f16 subnormals, an absolute error below 2^-25), and H is stored in
+ * f16 (finer than the bf16 layer's H).  A finite activation or H value past
+ * +-65504 has no f16 form: the call then records MOE_ERR_DEVICE in the
+ * device status and its results are not valid. */
 
 /* Quantise n_mat bf16 matrices of rows x cols each (contiguous, row-major):
  * per matrix scale = amax / 448 in fp32 (1 if the matrix is all zero), code =
@@ -280,7 +285,9 @@ int moe_quantize_fp8(const void* w, int32_t n_mat, int64_t rows, int64_t cols, u
  *   w_gate, w_up [E+S, F, d] and w_down [E+S, d, F] E4M3 codes
  *   scales [3, E+S] fp32: gate, up and down scale of each expert
  *   counts [E] required (kept rows per routed expert)
- * Other arguments as moe_expert_ffn. */
+ * The f16 token copies go into the workspace (its x_perm and y_perm regions),
+ * so x_perm may not be the workspace's own x_perm (moe_workspace_views):
+ * MOE_ERR_INVALID_ARG.  Other arguments as moe_expert_ffn. */
 int moe_expert_ffn_fp8(const moe_config* cfg, const void* x, const void* x_perm,
                        const int32_t* offsets, const int32_t* counts, const uint8_t* w_gate,
                        const uint8_t* w_up, const uint8_t* w_down, const float* scales,

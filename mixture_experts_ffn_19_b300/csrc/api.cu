@@ -161,6 +161,16 @@ int ffn_impl(const moe_config* c, const void* x, const void* x_perm, const int32
   fp.tile_ctr = at<int>(ws, L.tile_ctr);
   fp.num_sms = num_sms();
   fp.w_scales = w_scales;
+  if (w_scales) {
+    // f16 token copies for the E4M3 GEMMs: the routed rows in the workspace's
+    // x_perm (in place when the caller's x_perm is that buffer, as in
+    // moe_forward_fp8), the shared experts' copy of x past the routed rows of
+    // the workspace's y_perm, which the down GEMM only writes afterwards
+    fp.tok16 = at<void>(ws, L.x_perm);
+    fp.x16 = c->n_shared > 0 ? static_cast<void*>(at<char>(ws, L.y_perm) +
+                                                  (size_t)max_rows_of(c) * c->d_model * 2)
+                             : at<void>(ws, L.x_perm);
+  }
   const cudaError_t err = c->dtype == MOE_BF16 ? launch_ffn_tc(fp, s, mid) : launch_ffn_simt(fp, s, mid);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -424,6 +434,9 @@ int moe_expert_ffn_fp8(const moe_config* c, const void* x, const void* x_perm,
   if ((st = check_ws(c, ws, ws_bytes)) != MOE_OK) return st;
   if (!x || !x_perm || !offsets || !counts || !y_perm) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(x_perm) || !aligned16(y_perm)) return MOE_ERR_INVALID_ARG;
+  // the call writes f16 copies of the token rows into the workspace's x_perm
+  const Layout L = layout_of(c);
+  if (x_perm == at<void>(ws, L.x_perm)) return MOE_ERR_INVALID_ARG;
   if (c->n_tokens == 0) return MOE_OK;
   return ffn_impl(c, x, x_perm, offsets, counts, w_gate, w_up, w_down, nullptr, nullptr, scales,
                   y_perm, ws, static_cast<cudaStream_t>(stream), nullptr);

@@ -293,6 +293,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
          | (static_cast<uint32_t>(m >> 4) << 24); // M / 16
 }
 
+// The same for f16 A and B (both operands of one MMA always share a type).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
+  return (1u << 4)                                // D format: f32
+         | (static_cast<uint32_t>(n >> 3) << 17)  // N / 8 (A, B format 0: f16)
+         | (static_cast<uint32_t>(m >> 4) << 24); // M / 16
+}
+
 // Load 32 consecutive 32-bit columns of this warp's 32 TMEM lanes.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(

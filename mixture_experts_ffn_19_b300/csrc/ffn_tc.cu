@@ -22,6 +22,7 @@
 // tiles fastest, so CTAs running together share one weight tile through L2.
 // Every wait is bounded (kWaitLimitNs); on time-out the CTA records
 // MOE_ERR_TIMEOUT in the status word, stops issuing work and frees its TMEM.
+#include <algorithm>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -335,11 +336,13 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ 
 // fastest, so a weight tile is read from HBM once.
 //
 // FP8 weights (W8): the weight tile arrives as E4M3 codes (8 KB per stage, half
-// the HBM bytes) in a staging buffer; four converter warps widen it to bf16 in
+// the HBM bytes) in a staging buffer; four converter warps widen it to f16 in
 // the 128-byte-swizzled layout the MMA reads (every E4M3 value is exact in
-// bf16) and release the stage to the MMA warp; the per-expert-matrix scales
-// multiply the accumulators in the epilogue («大模型MoE架构揭秘» §5.4: expert
-// weights in low precision with per-expert scales, router in high precision).
+// f16; one conversion per code pair, against three for bf16) and release the
+// stage to the MMA warp, which multiplies f16 by f16: the token rows and H are
+// f16 copies in this path.  The per-expert-matrix scales multiply the
+// accumulators in the epilogue («大模型MoE架构揭秘» §5.4: expert weights in low
+// precision with per-expert scales, router in high precision).
 
 namespace swp {
 
@@ -352,6 +355,7 @@ constexpr int TMEM_COLS = 128;                 // two 64-column accumulators
 constexpr int XS = TOK + 1;                    // exchange row (floats), conflict-free
 constexpr int MAX_STAGES = 10;
 constexpr int CONV_WARPS = 4;                  // W8 converter warps 6..9
+constexpr float kF16Max = 65504.f;             // largest finite f16
 
 // bf16 weights: one ring of [A (bf16 weights) | B (tokens)] stages, 64 deep
 // in K.  E4M3 weights: stages 128 deep in K, so every weight row is read as
@@ -407,19 +411,18 @@ struct Params {
   const float* scale1;           // W8: per-segment scales of the up weights (GEMM-1)
 };
 
-// 8 E4M3 codes -> 8 bf16 (exact: E4M3 -> f16 -> f32 -> bf16 never rounds).
-// The conversion unit does it in four instructions per pair; integer bit
-// moves measured slower on this part.
-__device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint2 v) {
+// 8 E4M3 codes -> 8 f16 (exact: every E4M3 value, subnormals included, is an
+// f16 normal), one conversion-unit instruction per pair.  Widening to bf16
+// instead took three per pair (through f32) and kept the converter warps
+// 7-9 % of the decode step longer.
+__device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint2 v) {
   uint32_t w[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t word = i < 2 ? v.x : v.y;
     const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((word >> (16 * (i & 1))) & 0xFFFFu);
     const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-    const __nv_bfloat162 b = __float22bfloat162_rn(f);
-    w[i] = *reinterpret_cast<const uint32_t*>(&b);
+    w[i] = *reinterpret_cast<const uint32_t*>(&hr);   // the pair as one register
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
@@ -561,7 +564,8 @@ ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_consta
         int seg, fb, ch;
         coord(T, seg, fb, ch);
         const int nt = min(TOK, seg_rows(p, seg) - ch * TOK);
-        const uint32_t idesc = idesc_bf16_f32(BM, (nt + 15) / 16 * 16);
+        const uint32_t idesc = W8 ? idesc_f16_f32(BM, (nt + 15) / 16 * 16)
+                                  : idesc_bf16_f32(BM, (nt + 15) / 16 * 16);
         const uint32_t buf = it & 1, use = it >> 1;
         if (!mbar_wait(&ctrl->tempty[buf], (use & 1) ^ 1, abort, p.status)) break;
         tc_fence_after();
@@ -630,7 +634,7 @@ ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_consta
 #pragma unroll
         for (int pass = 0; pass < PASSES; ++pass) {
           const int r = pass * ROWS_PER_PASS + (ct >> 4);
-          *reinterpret_cast<uint4*>(a_s + r * 128 + ((c ^ (r & 7)) << 4)) = e4m3x8_to_bf16x8(v[pass]);
+          *reinterpret_cast<uint4*>(a_s + r * 128 + ((c ^ (r & 7)) << 4)) = e4m3x8_to_f16x8(v[pass]);
         }
         fence_proxy_async_smem();
         mbar_arrive(&ctrl->conv[s2]);
@@ -683,14 +687,23 @@ ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_consta
             tmem_ld32(taddr + c * 32, g);
             tmem_wait_ld();
             if (col < p.n_out) {
+              bool over = false;
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
                 const int t = c * 32 + i;
                 if (t < nt) {
                   const float h = silu_f(__uint_as_float(g[i]) * sg) * xch[f * XS + t];
-                  p.out[(size_t)(row0 + t) * p.n_out + col] = __float2bfloat16_rn(h);
+                  const size_t o = (size_t)(row0 + t) * p.n_out + col;
+                  if (W8) {
+                    // H feeds the down GEMM as f16: a value past its range is an error
+                    over |= fabsf(h) > kF16Max;
+                    reinterpret_cast<__half*>(p.out)[o] = __float2half_rn(h);
+                  } else {
+                    p.out[o] = __float2bfloat16_rn(h);
+                  }
                 }
               }
+              if (W8 && over) set_status(p.status, kDevBadState);
             }
           }
           mbar_arrive(&ctrl->xempty);            // the next tile may overwrite xch
@@ -744,13 +757,14 @@ cudaError_t get_encoder() {
   return g_encode ? cudaSuccess : cudaErrorNotSupported;
 }
 
-// 2-D bf16 map over a row-major [rows, cols] matrix, box [box_rows, 64], 128B swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// 2-D bf16 (or f16) map over a row-major [rows, cols] matrix, box [box_rows, 64], 128B swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+              CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols * 2};
   const cuuint32_t box[2] = {BK, box_rows};
   const cuuint32_t elem[2] = {1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  return g_encode(m, dt, 2, const_cast<void*>(base), dims, strides,
                   box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -773,6 +787,83 @@ bool make_map8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, u
 }  // namespace
 
 namespace {
+
+// E4M3 path: f16 copies of the token rows the gate/up GEMM reads, so that its
+// MMAs take f16 on both sides.  Routed rows keep x_perm's row indices
+// (segment e's valid rows are offsets[e] .. offsets[e] + counts[e] - 1), and
+// the shared experts read an f16 copy of x.  One CTA per row; the valid rows
+// are numbered through a prefix sum of counts, so padding rows cost nothing.
+// bf16 -> f16 is exact from 2^-14 to 65504; a finite value past 65504 is an
+// error (status), as for H.  xp and xp16 may be the same buffer: a thread
+// loads all of its vectors of the row, then rewrites the same 16-byte pieces.
+// A row outside [0, max_rows) (inconsistent offsets and counts from a caller)
+// is skipped and reported.
+constexpr int kCvtThreads = 256, kCvtBatch = 4;
+__global__ void __launch_bounds__(kCvtThreads)
+tokens_f16_kernel(const __nv_bfloat16* xp, __half* xp16, const __nv_bfloat16* x, __half* x16,
+                  const int32_t* offsets, const int32_t* counts, int E, int N, int d, int shared,
+                  int64_t max_rows, int* status) {
+  griddep_wait();
+  __shared__ int pre[kMaxExperts + 1];
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int e = 0; e < E; ++e) { pre[e] = run; run += min(max(counts[e], 0), N); }
+    pre[E] = run;
+  }
+  __syncthreads();
+  const int routed = pre[E];
+  const int total = routed + (shared ? N : 0);
+  const int nvec = d / 8;
+  bool over = false;
+  for (int i = blockIdx.x; i < total; i += gridDim.x) {
+    const uint4* src;
+    uint4* dst;
+    if (i < routed) {
+      int lo = 0, hi = E - 1;   // the last segment whose first valid row number is <= i
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= i) lo = mid; else hi = mid - 1;
+      }
+      const int64_t r = (int64_t)offsets[lo] + (i - pre[lo]);
+      if (r < 0 || r >= max_rows) {
+        if (threadIdx.x == 0) set_status(status, kDevBadState);
+        continue;
+      }
+      src = reinterpret_cast<const uint4*>(xp + (size_t)r * d);
+      dst = reinterpret_cast<uint4*>(xp16 + (size_t)r * d);
+    } else {
+      const size_t row = (size_t)(i - routed);
+      src = reinterpret_cast<const uint4*>(x + row * d);
+      dst = reinterpret_cast<uint4*>(x16 + row * d);
+    }
+    for (int v0 = threadIdx.x; v0 < nvec; v0 += kCvtThreads * kCvtBatch) {
+      uint4 a[kCvtBatch];
+#pragma unroll
+      for (int u = 0; u < kCvtBatch; ++u) {
+        const int v = v0 + u * kCvtThreads;
+        if (v < nvec) a[u] = src[v];
+      }
+#pragma unroll
+      for (int u = 0; u < kCvtBatch; ++u) {
+        const int v = v0 + u * kCvtThreads;
+        if (v >= nvec) continue;
+        const uint32_t in[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+        uint32_t out[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&in[j]));
+          over |= (isfinite(f.x) && fabsf(f.x) > swp::kF16Max) ||
+                  (isfinite(f.y) && fabsf(f.y) > swp::kF16Max);
+          const __half2 h = __floats2half2_rn(f.x, f.y);
+          out[j] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        dst[v] = make_uint4(out[0], out[1], out[2], out[3]);
+      }
+    }
+  }
+  if (over) set_status(status, kDevBadState);
+  griddep_launch_dependents();
+}
 
 // Swap-AB (weights as the M operand) when experts see few tokens: decode-sized
 // batches, where 128-row token tiles would be mostly padding.  E4M3 weights
@@ -798,9 +889,27 @@ cudaError_t launch_swap(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) {
   auto wmap = [&](CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box) {
     return W8 ? make_map8(m, base, rows, cols, box) : make_map(m, base, rows, cols, box);
   };
+  // E4M3 weights: the MMAs take f16 tokens (f16 copies made here) and f16 H
+  const CUtensorMapDataType tdt = W8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const void* tok = W8 ? p.tok16 : p.x_perm;
+  const void* xs = W8 ? p.x16 : p.x;
+  if (W8) {
+    if (!p.tok16 || !p.x16) return cudaErrorInvalidValue;
+    const int64_t rows = (int64_t)p.N * p.k + (p.S > 0 ? p.N : 0);
+    int grid = (int)std::min<int64_t>(rows, 8LL * p.num_sms);
+    if (grid < 1) grid = 1;
+    if ((err = launch_chained(tokens_f16_kernel, grid, kCvtThreads, 0, s,
+                              static_cast<const __nv_bfloat16*>(p.x_perm), static_cast<__half*>(p.tok16),
+                              static_cast<const __nv_bfloat16*>(p.x), static_cast<__half*>(p.x16),
+                              p.offsets, p.counts, p.E, p.N, p.d, p.S > 0 ? 1 : 0,
+                              p.max_rows, p.status)) !=
+        cudaSuccess)
+      return err;
+    count_launch();
+  }
   CUtensorMap b0, b1, a0, a1;
-  if (!make_map(&b0, p.x_perm, (uint64_t)p.max_rows, p.d, swp::TOKB) ||
-      !make_map(&b1, p.x, (uint64_t)p.N, p.d, swp::TOKB) ||
+  if (!make_map(&b0, tok, (uint64_t)p.max_rows, p.d, swp::TOKB, tdt) ||
+      !make_map(&b1, xs, (uint64_t)p.N, p.d, swp::TOKB, tdt) ||
       !wmap(&a0, p.w_gate, (uint64_t)ET * p.F, p.d, swp::BM / 2) ||
       !wmap(&a1, p.w_up, (uint64_t)ET * p.F, p.d, swp::BM / 2))
     return cudaErrorInvalidValue;
@@ -812,7 +921,7 @@ cudaError_t launch_swap(const FfnParams& p, cudaStream_t s, cudaEvent_t mid) {
     return err;
   count_launch();
   if (mid) cudaEventRecord(mid, s);
-  if (!make_map(&b0, p.h, (uint64_t)p.max_total_rows, p.F, swp::TOKB) ||
+  if (!make_map(&b0, p.h, (uint64_t)p.max_total_rows, p.F, swp::TOKB, tdt) ||
       !wmap(&a0, p.w_down, (uint64_t)ET * p.d, p.F, swp::BM))
     return cudaErrorInvalidValue;
   swp::Params t2{p.E, p.S, p.N, p.F, p.d, (p.d + swp::BM - 1) / swp::BM, p.offsets, p.counts,

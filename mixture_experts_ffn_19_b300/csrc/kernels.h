@@ -137,6 +137,11 @@ struct FfnParams {
   // E4M3 weights: w_gate / w_up / w_down hold codes and w_scales [3][E+S] the
   // gate, up and down scale of each expert; null for bf16 weights
   const float* w_scales;
+  // E4M3 weights: f16 copies of the token rows the gate/up GEMM reads, at
+  // x_perm's row indices ([max_rows, d]; may be x_perm itself) and of x for
+  // the shared experts ([N, d]); H is then f16 as well
+  void* tok16;
+  void* x16;
 };
 
 struct CombineParams {

@@ -124,3 +124,18 @@ def test_zero_tokens_and_tiny_shapes_size_without_error(lib):
 def test_selftest_rejects_missing_workspace(lib):
     # host-side checks only: nothing is launched
     assert lib.moe_selftest_timeout(None, 0, 1000, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_fp8_ffn_refuses_the_workspace_x_perm(lib):
+    # the E4M3 expert FFN writes f16 copies of the token rows into the
+    # workspace's own x_perm, so that buffer cannot also be the input; the
+    # check is made before any launch (fake device addresses, nothing is read)
+    c = moe.make_config(32, 256, 8, 2, 512)
+    n = moe.moe_workspace_size(c)
+    ws = 1 << 36
+    v = moe.moe_views()
+    assert lib.moe_workspace_views(ctypes.byref(c), ws, n, ctypes.byref(v)) == moe.MOE_OK
+    fake = 1 << 40
+    st = lib.moe_expert_ffn_fp8(ctypes.byref(c), fake, v.x_perm, fake, fake, fake, fake, fake,
+                                fake, fake, ws, n, None)
+    assert st == moe.MOE_ERR_INVALID_ARG

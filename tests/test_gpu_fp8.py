@@ -203,3 +203,27 @@ def test_fp8_rejects_unsupported(cuda):
         moe.moe_quantize_fp8(torch.zeros((1, 3, 5), dtype=torch.bfloat16, device=cuda),
                              torch.zeros((1, 3, 5), dtype=torch.uint8, device=cuda),
                              torch.zeros(1, device=cuda))
+
+
+def test_fp8_activation_past_f16_range_is_reported(cuda):
+    """The E4M3 path multiplies f16 copies of the token rows: a finite value
+    past 65504 has no f16 form, so it sets the device status; the next call on
+    the same workspace starts clean."""
+    w = synth.small_workload("decode_mixtral", d_model=512, d_ff=1024)
+    inp = synth.make_inputs(w, with_experts=False)
+    wdev = upload_experts(w, cuda)
+    cfg = config_of(w)
+    ws = moe.alloc_workspace(cfg, cuda)
+    qd, sd = quantize_all(wdev, cuda)
+    xd = to_dev(inp["x"])
+    y = torch.zeros((w.n_tokens, w.d_model), dtype=torch.bfloat16, device=cuda)
+    rest = (to_dev(inp["w_router"]), to_dev(inp["router_bias"]), qd["w_gate"], qd["w_up"],
+            qd["w_down"], sd, y, None, ws)
+    moe.moe_forward_fp8(cfg, xd, *rest)
+    assert moe.moe_device_status(ws) == moe.MOE_OK
+    big = xd.clone()
+    big[3, 7] = 1.0e5
+    moe.moe_forward_fp8(cfg, big, *rest)
+    assert moe.moe_device_status(ws) == moe.MOE_ERR_DEVICE
+    moe.moe_forward_fp8(cfg, xd, *rest)
+    assert moe.moe_device_status(ws) == moe.MOE_OK
