@@ -212,20 +212,52 @@ def gemm1_kernel(w) -> str:
     return "ffn_tc_kernel<0>"
 
 
+def strip_c_comments(text: str) -> str:
+    """C/C++/CUDA source without its comments, every whitespace run collapsed to
+    one space (string and character literals kept as written)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":                               # literal: copy through its closing quote
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+            out.append(" ")
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def code_digest(srcs) -> str:
+    """sha256 of the sources' code (comments and layout left out): an edit of a
+    comment keeps an ncu capture valid, any change to the code voids it."""
+    import hashlib
+    h = hashlib.sha256()
+    for src in srcs:
+        with open(os.path.join(ROOT, src), encoding="utf-8") as f:
+            h.update(strip_c_comments(f.read()).encode())
+    return h.hexdigest()
+
+
 def measured_traffic(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` on `workload` from a committed ncu capture
-    (profiles/ncu_traffic.json), or None when there is none or the kernel's source
-    has changed since it was taken (sha256 of its source files)."""
-    import hashlib
+    (profiles/ncu_traffic.json), or None when there is none or the kernel's code
+    has changed since it was taken (code_digest of its source files)."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             entry = json.load(f)[workload][kernel]
-        h = hashlib.sha256()
-        for src in entry["sources"]:
-            with open(os.path.join(ROOT, src), "rb") as f:
-                h.update(f.read())
-        if h.hexdigest() != entry["source_sha256"]:
+        if code_digest(entry["sources"]) != entry["source_sha256"]:
             return None
         return float(entry["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
@@ -243,18 +275,13 @@ TRAFFIC_SOURCES = {
 
 def record_traffic(workload: str, kernel: str, nbytes: float, command: str) -> None:
     """Store one ncu capture's DRAM bytes per launch in profiles/ncu_traffic.json with
-    the sha256 of the kernel's sources (read back by measured_traffic)."""
-    import hashlib
+    the code digest of the kernel's sources (read back by measured_traffic)."""
     srcs = TRAFFIC_SOURCES[kernel]
-    h = hashlib.sha256()
-    for s in srcs:
-        with open(os.path.join(ROOT, s), "rb") as f:
-            h.update(f.read())
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     data = json.load(open(path)) if os.path.exists(path) else {}
     data.setdefault(workload, {})[kernel] = {
         "dram_bytes_per_launch": float(nbytes), "sources": srcs,
-        "source_sha256": h.hexdigest(), "command": command}
+        "source_sha256": code_digest(srcs), "command": command}
     with open(path, "w") as f:
         json.dump(data, f, indent=1, sort_keys=True)
 

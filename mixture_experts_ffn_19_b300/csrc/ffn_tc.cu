@@ -361,7 +361,7 @@ constexpr float kF16Max = 65504.f;             // largest finite f16
 // in K.  E4M3 weights: stages 128 deep in K, so every weight row is read as
 // a whole 128-byte line (64-byte pieces of rows 8 KB apart held the DRAM
 // below half its bandwidth): a TMA ring of [B (2 K-chunks) | E4M3 tile]
-// stages and a ring of converted stages of two bf16 A tiles.
+// stages and a ring of converted stages of two f16 A tiles.
 template <bool W8>
 struct Shape {
   static constexpr int KSUB = W8 ? 2 : 1;               // 64-deep K-chunks per stage
@@ -376,7 +376,7 @@ struct Shape {
 struct Ctrl {
   uint64_t full[MAX_STAGES];
   uint64_t empty[MAX_STAGES];
-  uint64_t conv[4];              // W8: converted bf16 tile ready
+  uint64_t conv[4];              // W8: converted f16 tile ready
   uint64_t afree[4];             // W8: converted tile consumed by the MMA
   uint64_t tfull[2];
   uint64_t tempty[2];
@@ -438,8 +438,9 @@ ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_consta
                    Params p) {
   griddep_wait();
   if (MOE_GEMM_EARLY_TRIGGER) griddep_launch_dependents();
-  // tmB0/tmB1: token rows (x_perm / x for GEMM-1, H for GEMM-2);
-  // tmA0/tmA1: weights (gate / up for GEMM-1, down for GEMM-2), bf16 or E4M3
+  // tmB0/tmB1: token rows (x_perm / x for GEMM-1, H for GEMM-2; their f16
+  // copies with E4M3 weights); tmA0/tmA1: weights (gate / up for GEMM-1,
+  // down for GEMM-2), bf16 or E4M3
   constexpr int STAGES = Shape<W8>::STAGES, STAGE_BYTES = Shape<W8>::STAGE_BYTES;
   constexpr int A_STAGES = Shape<W8>::A_STAGES, KSUB = Shape<W8>::KSUB;
   constexpr int TOK = Shape<W8>::TOK, B_BYTES = Shape<W8>::B_BYTES;
@@ -599,7 +600,7 @@ ffn_tc_swap_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_consta
       }
     }
   } else if (W8 && warp >= 6 && warp < 6 + CONV_WARPS) {
-    // converter warps: E4M3 staging tile (128 rows x 128 codes) -> two bf16
+    // converter warps: E4M3 staging tile (128 rows x 128 codes) -> two f16
     // tiles in the 128-byte swizzled K-major layout (16-byte chunk c of row r
     // at chunk c ^ (r & 7)); 16 threads per row, 2 * CONV_WARPS rows per pass
     constexpr int ROWS_PER_PASS = 2 * CONV_WARPS;
@@ -771,7 +772,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 }
 
 // 2-D E4M3 map over a row-major [rows, cols] byte matrix, box [box_rows, 128]
-// (whole 128-byte lines), no swizzle (the converter warps lay the bf16 tiles
+// (whole 128-byte lines), no swizzle (the converter warps lay the f16 tiles
 // out themselves).
 bool make_map8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   const cuuint64_t dims[2] = {cols, rows};

@@ -77,3 +77,18 @@ def test_gemm1_roofline_picks_binding_bound():
     r2 = bench.gemm1_roofline(wd, np.full(8, 16), 128, 2 * 128 * 4096 * 2 * 14336, 0.33, 0.1,
                               {"sm_mhz": 2032, "reasons": []}, pk)
     assert r2["bound"] == "hbm" and r2["unit"] == "GB/s"
+
+
+def test_traffic_records_follow_code_not_comments(tmp_path, monkeypatch):
+    # an ncu capture stays valid through comment and layout edits of the
+    # kernel's sources and lapses with any change to the code itself
+    assert bench.strip_c_comments('a = 1; // x\n/* y\n */  b = "//z/*";\nc = \'"\';') == \
+        'a = 1; b = "//z/*"; c = \'"\';'
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    src = tmp_path / "k.cu"
+    src.write_text("int f(int a) {\n  return a + 1;  // one more\n}\n")
+    d0 = bench.code_digest(["k.cu"])
+    src.write_text("/* header */\nint f(int a) {\n    return a + 1;  // plus one\n}\n")
+    assert bench.code_digest(["k.cu"]) == d0
+    src.write_text("int f(int a) {\n  return a + 2;  // one more\n}\n")
+    assert bench.code_digest(["k.cu"]) != d0
