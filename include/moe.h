@@ -267,9 +267,9 @@ int moe_router_bias_update(const moe_config* cfg, const void* workspace, size_t 
  * is fp32.  The tensor cores take the codes widened to f16 (exact) times f16
  * copies of the bf16 token rows (exact from 2^-14 to 65504; smaller values
  * round to f16 subnormals, an absolute error below 2^-25), and H is stored in
- * f16 (finer than the bf16 layer's H).  A finite activation or H value past
- * +-65504 has no f16 form: the call then records MOE_ERR_DEVICE in the
- * device status and its results are not valid. */
+ * f16 (finer than the bf16 layer's H).  A finite token value past +-65504,
+ * or an H value past it (infinities included), has no f16 form: the call then
+ * records MOE_ERR_DEVICE in the device status and its results are not valid. */
 
 /* Quantise n_mat bf16 matrices of rows x cols each (contiguous, row-major):
  * per matrix scale = amax / 448 in fp32 (1 if the matrix is all zero), code =
