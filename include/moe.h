@@ -294,7 +294,9 @@ int moe_expert_ffn_fp8(const moe_config* cfg, const void* x, const void* x_perm,
                        void* y_perm, void* workspace, size_t workspace_bytes, void* stream);
 
 /* moe_forward with E4M3 expert weights (same conditions as
- * moe_expert_ffn_fp8); the router runs on the bf16 w_router as in moe_forward. */
+ * moe_expert_ffn_fp8); the router runs on the bf16 w_router as in moe_forward.
+ * Afterwards the workspace's x_perm (moe_workspace_views) holds the f16 copies
+ * of the kept token rows, and its H is f16. */
 int moe_forward_fp8(const moe_config* cfg, const void* x, const void* w_router,
                     const float* router_bias, const uint8_t* w_gate, const uint8_t* w_up,
                     const uint8_t* w_down, const float* scales, void* y, const moe_stats* stats,
