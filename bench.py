@@ -7,7 +7,7 @@ A step is one moe_forward (router -> dispatch -> expert GEMMs -> combine) over
 one batch of the workload, inputs resident in HBM.  L2 is flushed between
 steps (a 512 MB write, outside the timed events).  With --gpus N > 1 (launched
 by torch.distributed.run) every rank runs an independent replica on its own
-GPU: the layer has no exchange step in this build, so there is no collective
+GPU: the single-GPU layer has no exchange step, so there is no collective
 on the data path; the barrier and the max over ranks of the timed region are
 the only cross-rank steps.
 
@@ -683,9 +683,9 @@ def time_e2e(layer, steps, warmup, flush, world):
             f"not flushed: {weight_bytes / 1e9:.2f} GB of expert weights streamed per step"}
 
 
-# Workloads timed beside the headline in the default run, with the figure each
-# one is judged by (the decode layers by the HBM fraction of the weights they
-# stream, the prefill layers by the gate/up GEMM's roofline).
+# Workloads timed beside the headline in the default run, each with the figure
+# that bounds it (the decode layers: the HBM fraction of the weights they
+# stream; the prefill layers: the gate/up GEMM's roofline).
 SECONDARY = ["decode_mixtral", "decode_dsv2", "dsv2", "e64_reroute"]
 
 
