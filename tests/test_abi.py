@@ -139,3 +139,14 @@ def test_fp8_ffn_refuses_the_workspace_x_perm(lib):
     st = lib.moe_expert_ffn_fp8(ctypes.byref(c), fake, v.x_perm, fake, fake, fake, fake, fake,
                                 fake, fake, ws, n, None)
     assert st == moe.MOE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("n,e,k,s", [(1, 1, 1, 1), (32, 160, 6, 2), (64, 8, 2, 1), (127, 4, 4, 3),
+                                      (300, 64, 2, 1), (4097, 256, 8, 8)])
+def test_shared_f16_copy_fits_past_the_routed_rows(lib, n, e, k, s):
+    # with E4M3 weights the shared experts read an f16 copy of x placed in
+    # y_perm after the routed region: rows [max_rows, max_rows + N) must exist
+    c = moe.make_config(n, 64, e, k, 64, n_shared=s)
+    assert moe.moe_max_total_rows(c) >= moe.moe_max_rows(c) + n
+    # and the routed rows a dispatch can produce stay inside max_rows
+    assert moe.moe_max_rows(c) >= n * k + e * 127
